@@ -1,0 +1,82 @@
+"""Seeded synthetic inputs for the W4A16 QKV projection and the dense f16 matmul.
+
+This module only draws random numbers. It holds none of the method's
+arithmetic: packed weights are drawn as uniformly random 32-bit words, which is
+the same thing as drawing the eight 4-bit fields of each word independently and
+uniformly (every 4-bit pattern, i.e. every signed value in [-8, 7], is equally
+likely). Unpacking, dequantisation and the products live elsewhere.
+
+Distributions (workload shapes of the W4A16 projection and the dense matmul):
+
+- ``x``: f16, standard normal, rounded to f16 by the dtype cast.
+- ``wq``/``wk``/``wv``: uint32 ``[K/8, N]``, uniform over all 2**32 words.
+- ``sq``/``sk``/``sv``: f16 ``[K/128, N]``, uniform in [0.005, 0.02].
+- dense ``a``/``b``: f16, uniform in [-1, 1]; backward ``g``: f16 standard normal.
+
+One ``numpy.random.Generator`` (PCG64) per call, seeded by ``seed``; tensors
+are drawn in the fixed order x, wq, wk, wv, sq, sk, sv.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import numpy as np
+
+GROUP_SIZE = 128
+
+
+@dataclass
+class QKVInputs:
+    x: np.ndarray   # f16 [M, K]
+    wq: np.ndarray  # u32 [K/8, N]
+    wk: np.ndarray
+    wv: np.ndarray
+    sq: np.ndarray  # f16 [K/128, N]
+    sk: np.ndarray
+    sv: np.ndarray
+
+    @property
+    def shape(self):
+        m, k = self.x.shape
+        return m, self.wq.shape[1], k
+
+    def weights(self):
+        return (self.wq, self.wk, self.wv)
+
+    def scales(self):
+        return (self.sq, self.sk, self.sv)
+
+
+def qkv_inputs(m: int, n: int, k: int, seed: int = 0,
+               scale_lo: float = 0.005, scale_hi: float = 0.02) -> QKVInputs:
+    """Draw one W4A16 problem of shape (M, N, K)."""
+    if k % GROUP_SIZE:
+        raise ValueError(f"K={k} is not a multiple of {GROUP_SIZE}")
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((m, k), dtype=np.float32).astype(np.float16)
+    w = [rng.integers(0, 2**32, size=(k // 8, n), dtype=np.uint32) for _ in range(3)]
+    s = [rng.uniform(scale_lo, scale_hi, size=(k // GROUP_SIZE, n)).astype(np.float16)
+         for _ in range(3)]
+    return QKVInputs(x, w[0], w[1], w[2], s[0], s[1], s[2])
+
+
+def weight_sets(n: int, k: int, count: int, seed: int = 1):
+    """``count`` distinct (wq, wk, wv, sq, sk, sv) sets, used to rotate weights
+    between timed launches so that every launch streams its weights from HBM."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for _ in range(count):
+        w = [rng.integers(0, 2**32, size=(k // 8, n), dtype=np.uint32) for _ in range(3)]
+        s = [rng.uniform(0.005, 0.02, size=(k // GROUP_SIZE, n)).astype(np.float16)
+             for _ in range(3)]
+        out.append((*w, *s))
+    return out
+
+
+def dense_inputs(m: int, n: int, k: int, seed: int = 0):
+    """A f16[M,K], B f16[K,N] uniform in [-1,1] and G f16[M,N] ~ N(0,1)."""
+    rng = np.random.default_rng(seed)
+    a = rng.uniform(-1.0, 1.0, size=(m, k)).astype(np.float16)
+    b = rng.uniform(-1.0, 1.0, size=(k, n)).astype(np.float16)
+    g = rng.standard_normal((m, n), dtype=np.float32).astype(np.float16)
+    return a, b, g
