@@ -1,0 +1,474 @@
+"""Benchmark of the W4A16 fused QKV projection (and the dense tensor-core matmul).
+
+One step = one pass of the hot path over one batch: one kaio_qkv_project_int4
+call (Q, K and V together) on the chosen workload. Default workload: the decode
+projection M=1, K=N=4096 (25.95 MB of packed weights and scales per step).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl kaio|reference]
+
+Prints one JSON line (rank 0). Under torchrun (N > 1) every rank runs an
+independent replica on its own GPU (the projection has no exchange step) and
+the value is the total over ranks divided by the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+DEFAULT_STEPS = {
+    "qkv_decode_m1_k4096_n4096": 100000,
+    "qkv_m16_k256_n128": 100000,
+    "qkv_batched_decode_m16_k8192_n8192": 40000,
+    "qkv_prefill_m4096_k4096_n4096": 2000,
+    "matmul_f16_m4096_n4096_k4096_fwd_bwd": 1000,
+}
+CONFIGS = {
+    # name: (kind, M, N, K)
+    "qkv_decode_m1_k4096_n4096": ("qkv", 1, 4096, 4096),
+    "qkv_m16_k256_n128": ("qkv", 16, 128, 256),
+    "qkv_batched_decode_m16_k8192_n8192": ("qkv", 16, 8192, 8192),
+    "qkv_prefill_m4096_k4096_n4096": ("qkv", 4096, 4096, 4096),
+    "matmul_f16_m4096_n4096_k4096_fwd_bwd": ("matmul", 4096, 4096, 4096),
+}
+DEFAULT_CONFIG = "qkv_decode_m1_k4096_n4096"
+METRIC = "W4A16 QKV TFLOP/s and weight GB/s (1xGB300) as % of roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_BYTES = 129 * 1024 * 1024
+
+
+def qkv_bytes(m, n, k):
+    weights = 3 * (k // 8) * n * 4 + 3 * (k // 128) * n * 2     # packed + scales
+    other = m * k * 2 + 3 * m * n * 2                             # x in, q/k/v out
+    return weights, other
+
+
+def qkv_flops(m, n, k):
+    return 3 * 2 * m * n * k
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def profile_traffic(kernel_file: str, config: str):
+    """DRAM bytes per launch from the committed ncu summary of this kernel and
+    workload, if that summary was taken from the current kernel source."""
+    src = os.path.join(ROOT, "qkv_projection_gb300", "csrc", kernel_file)
+    summary = os.path.join(ROOT, "profiles", f"{config}.md")
+    if not (os.path.exists(src) and os.path.exists(summary)):
+        return None
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    text = open(summary).read()
+    m_sha = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]{16})", text)
+    m_b = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not m_sha or not m_b or m_sha.group(1) != sha:
+        return None
+    return float(m_b.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu),
+                 "--query-gpu=clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+                 "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+                 "clocks_event_reasons.sw_power_cap",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.perf_counter(), line.strip()))
+
+    def mark(self, t0, t1):
+        self.window = (t0, t1)
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        mhz, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        w0, w1 = getattr(self, "window", (float("-inf"), float("inf")))
+        inside = [l for t, l in self.lines if w0 <= t <= w1]
+        for line in inside or [l for _, l in self.lines]:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 6:
+                continue
+            try:
+                mhz.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for name, v in zip(names, parts[2:6]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        if not mhz:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
+        mhz.sort()
+        return {"sm_mhz": mhz[len(mhz) // 2], "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(mhz)}
+
+
+# ---------------------------------------------------------------- distributed
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def dist_init(ws):
+    if ws <= 1:
+        return None
+    import torch.distributed as dist
+    backend = "nccl"
+    try:
+        import torch
+        if not torch.cuda.is_available():
+            backend = "gloo"
+    except Exception:
+        backend = "gloo"
+    dist.init_process_group(backend=backend)
+    return dist
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def max_over_ranks(dist, value, device):
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- kaio arm
+def run_kaio(args, cfg_name, ws, rank, local, dist):
+    import numpy as np
+    import torch
+
+    from qkv_projection_gb300 import kaio
+    from qkv_projection_gb300.inputs import dense_inputs, qkv_inputs, weight_sets
+
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    kind, M, N, K = CONFIGS[cfg_name]
+    peaks, peak_src = load_peaks()
+    stream = torch.cuda.Stream(device=device)
+
+    def dev(a):
+        a = np.ascontiguousarray(a)
+        if a.dtype == np.uint32:
+            a = a.view(np.int32)
+        return torch.from_numpy(a).to(device)
+
+    if kind == "qkv":
+        wbytes, obytes = qkv_bytes(M, N, K)
+        inp = qkv_inputs(M, N, K, seed=0)
+        # Rotate among weight sets totalling >= 3x L2 so each launch streams its
+        # weights from HBM (and at least 2 sets even when one set exceeds L2).
+        nsets = max(2, -(-3 * L2_BYTES // wbytes))
+        sets = [tuple(dev(a) for a in (inp.wq, inp.wk, inp.wv, inp.sq, inp.sk, inp.sv))]
+        for ws_ in weight_sets(N, K, nsets - 1, seed=1):
+            sets.append(tuple(dev(a) for a in ws_))
+        x = dev(inp.x)
+        outs = [torch.empty((M, N), dtype=torch.float16, device=device) for _ in range(3)]
+        lib = kaio.lib()
+        ptr_sets = [[t.data_ptr() for t in s] for s in sets]
+        xo = [x.data_ptr()] + [o.data_ptr() for o in outs]
+        sp = int(stream.cuda_stream)
+
+        def step(i):
+            w = ptr_sets[i % len(ptr_sets)]
+            st = lib.kaio_qkv_project_int4(xo[0], w[0], w[1], w[2], w[3], w[4], w[5],
+                                           xo[1], xo[2], xo[3], M, N, K, sp)
+            if st:
+                raise kaio.KaioError(st, kaio.last_error())
+
+        units_bytes = wbytes
+        alg_bytes = wbytes + obytes
+        flops = qkv_flops(M, N, K)
+        kernel_file = "decode_w4a16.cu" if kaio.qkv_path(M) == 0 else "tc_kernels.cu"
+        bound = "hbm" if M <= 16 else "tensor"
+        launches_per_step = 1
+    else:
+        a, b, g = dense_inputs(M, N, K, seed=0)
+        A, B, G = dev(a), dev(b), dev(g)
+        C = torch.empty((M, N), dtype=torch.float32, device=device)
+        dA = torch.empty((M, K), dtype=torch.float32, device=device)
+        dB = torch.empty((K, N), dtype=torch.float32, device=device)
+        lib = kaio.lib()
+        sp = int(stream.cuda_stream)
+
+        def step(i):
+            kaio.check(lib.kaio_matmul_tc(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K, sp))
+            kaio.check(lib.kaio_matmul_tc_backward(A.data_ptr(), B.data_ptr(), G.data_ptr(),
+                                                   dA.data_ptr(), dB.data_ptr(), M, N, K, sp))
+
+        wbytes = 0
+        units_bytes = 0
+        alg_bytes = 3 * (2 * M * K * 2 + M * N * 4)
+        flops = 3 * 2 * M * N * K
+        kernel_file = "tc_kernels.cu"
+        bound = "tensor"
+        launches_per_step = 3
+
+    # Warm-up (also allocates the decode workspace outside capture).
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, 3)):
+            step(i)
+    stream.synchronize()
+
+    # Capture up to `chunk` steps in one CUDA graph; replay it to cover K steps.
+    chunk = min(args.steps, 1000 if kind == "qkv" else 8)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(graph, stream=stream):
+            for i in range(chunk):
+                step(i)
+    stream.synchronize()
+    replays = -(-args.steps // chunk)
+    steps = replays * chunk
+    for _ in range(2):
+        graph.replay()
+    stream.synchronize()
+
+    barrier(dist)
+    torch.cuda.synchronize()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        time.sleep(0.3)
+        w0 = time.perf_counter()
+        ev0.record(stream)
+        for _ in range(replays):
+            graph.replay()
+        ev1.record(stream)
+        ev1.synchronize()
+        clk.mark(w0, time.perf_counter() + 0.05)
+        time.sleep(0.1)
+    torch.cuda.synchronize()
+    barrier(dist)
+    t_ms = ev0.elapsed_time(ev1)
+    t_max_ms = max_over_ranks(dist, t_ms, device)
+    per_step_s = t_max_ms / 1e3 / steps
+
+    # End to end through the public API: per step, copy x in from pinned host
+    # memory, run the projection, read the three outputs back.
+    e2e = None
+    if kind == "qkv" and not args.no_e2e:
+        hx = torch.from_numpy(inp.x.copy()).pin_memory()
+        ho = [torch.empty((M, N), dtype=torch.float16).pin_memory() for _ in range(3)]
+        xin = torch.empty_like(x)
+        e_steps = min(args.steps, 2000)
+        with torch.cuda.stream(stream):
+            for i in range(3):
+                xin.copy_(hx, non_blocking=True)
+                kaio.qkv_project_int4(xin, *sets[i % len(sets)], out=outs, stream=stream)
+                for o, h in zip(outs, ho):
+                    h.copy_(o, non_blocking=True)
+            stream.synchronize()
+            barrier(dist)
+            t0 = time.perf_counter()
+            for i in range(e_steps):
+                xin.copy_(hx, non_blocking=True)
+                kaio.qkv_project_int4(xin, *sets[i % len(sets)], out=outs, stream=stream)
+                for o, h in zip(outs, ho):
+                    h.copy_(o, non_blocking=True)
+            stream.synchronize()
+            t1 = time.perf_counter()
+        te = max_over_ranks(dist, t1 - t0, device)
+        e2e = {"value": round(ws * units_bytes * e_steps / te / 1e9, 3), "unit": "GB/s",
+               "h2d_bytes_per_step": M * K * 2, "d2h_bytes_per_step": 3 * M * N * 2,
+               "steps": e_steps, "weights_resident": True}
+
+    if rank != 0:
+        return None
+
+    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    tc_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))   # f16 = bf16 rate
+    if bound == "hbm":
+        achieved = alg_bytes / per_step_s / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 2), "peak": hbm_peak, "unit": "GB/s",
+                "frac": round(achieved / hbm_peak, 4), "peak_source": peak_src}
+    else:
+        achieved = flops / per_step_s / 1e12
+        roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": tc_peak, "unit": "TFLOP/s",
+                "frac": round(achieved / tc_peak, 4), "peak_source": peak_src + " bf16 burst (f16 = bf16 rate)"}
+    roof["traffic"] = profile_traffic(kernel_file, cfg_name)
+
+    if kind == "qkv":
+        value = ws * wbytes / per_step_s / 1e9
+        unit = "GB/s"
+    else:
+        value = ws * flops / per_step_s / 1e12
+        unit = "TFLOP/s"
+    line = {
+        "metric": METRIC if kind == "qkv" else "dense f16 tensor-core matmul fwd+bwd TFLOP/s",
+        "value": round(value, 3),
+        "unit": unit,
+        "n_gpus": ws,
+        "steps": steps,
+        "warmup": max(args.warmup, 3),
+        "ms_per_step": round(per_step_s * 1e3, 6),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f16 (int4 weights, f32 accumulate)" if kind == "qkv" else "f16 (f32 accumulate)",
+        "data": "synthetic (seeded; weights rotate over sets totalling >= 3x L2)",
+        "config": {"workload": cfg_name, "M": M, "N": N, "K": K, "parallelism": f"replicas x{ws}",
+                   "l2": "inputs larger than L2 (weight sets rotated)" if kind == "qkv" else
+                         "operands 32 MiB each; no flush (compute-bound)"},
+        "tflops": round(ws * flops / per_step_s / 1e12, 3),
+        "weight_gbs": round(ws * wbytes / per_step_s / 1e9, 3) if kind == "qkv" else None,
+        "roofline": roof,
+        "e2e": e2e,
+        "gpu_launches": steps * launches_per_step,
+        "clocks": clk.summary(),
+    }
+    if not args.no_cpu_baseline and ws == 1 and kind == "qkv":
+        line["cpu_baseline"] = cpu_baseline(cfg_name, budget_s=args.cpu_budget)
+    return line
+
+
+# ---------------------------------------------------------------- oracle arm
+def oracle_step_fn(cfg_name, frac):
+    """One oracle evaluation on a column sample (fraction `frac` of N)."""
+    import numpy as np
+
+    import oracle
+    from qkv_projection_gb300.inputs import qkv_inputs
+
+    kind, M, N, K = CONFIGS[cfg_name]
+    inp = qkv_inputs(M, N, K, seed=0)
+    ncols = max(8, int(round(N * frac)) // 8 * 8)
+    cols = np.arange(ncols)
+    sub = [inp.x] + [np.ascontiguousarray(w[:, cols]) for w in inp.weights()] + \
+          [np.ascontiguousarray(s[:, cols]) for s in inp.scales()]
+    wbytes = qkv_bytes(M, ncols, K)[0]
+
+    def step():
+        oracle.qkv_project_int4_ref(*sub)
+    return step, wbytes, ncols
+
+
+def cpu_baseline(cfg_name, budget_s=15.0):
+    kind, M, N, K = CONFIGS[cfg_name]
+    step, wb, ncols = oracle_step_fn(cfg_name, 1.0 if N * K <= 4096 * 4096 else 0.125)
+    t0 = time.perf_counter()
+    step()
+    one = time.perf_counter() - t0
+    reps = max(1, int(budget_s / max(one, 1e-6)))
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        step()
+    dt = time.perf_counter() - t0
+    return {"value": round(wb * reps / dt / 1e9, 4), "unit": "GB/s", "cores": os.cpu_count(),
+            "kind": "oracle",
+            "sample": f"{reps} oracle evaluations of {cfg_name} on {ncols} of {N} columns "
+                      f"(numpy float64; BLAS may use up to {os.cpu_count()} threads)"}
+
+
+def run_reference(args, cfg_name, ws, rank):
+    kind, M, N, K = CONFIGS[cfg_name]
+    if rank != 0:
+        return None
+    if kind != "qkv":
+        return {"impl": "reference", "unavailable": "oracle arm covers the W4A16 workloads only"}
+    # Size each step's sample so the whole run takes about a minute.
+    total_steps = args.steps + max(args.warmup, 3)
+    probe, _, _ = oracle_step_fn(cfg_name, 1.0 / 64)
+    t0 = time.perf_counter()
+    probe()
+    per_col = (time.perf_counter() - t0) / max(8, N // 64)
+    frac = min(1.0, max(8.0 / N, 60.0 / total_steps / max(per_col, 1e-9) / N))
+    step, wb, ncols = oracle_step_fn(cfg_name, frac)
+    for _ in range(max(args.warmup, 3)):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t0
+    value = wb * args.steps / dt / 1e9
+    sample = (f"each step: one oracle evaluation of {cfg_name} on {ncols} of {N} columns "
+              f"(numpy float64)")
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 5), "unit": "GB/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": max(args.warmup, 3),
+        "ms_per_step": round(dt / args.steps * 1e3, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+        "config": {"workload": cfg_name, "M": M, "N": N, "K": K},
+        "cpu_baseline": {"value": round(value, 5), "unit": "GB/s", "cores": os.cpu_count(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 5), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["kaio", "reference"], default="kaio")
+    ap.add_argument("--config", choices=sorted(CONFIGS), default=DEFAULT_CONFIG)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.steps is None:
+        args.steps = DEFAULT_STEPS[args.config]
+    ws, rank, local = dist_env()
+    if args.impl == "reference":
+        line = run_reference(args, args.config, ws, rank)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+    dist = dist_init(ws)
+    line = run_kaio(args, args.config, ws, rank, local, dist)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

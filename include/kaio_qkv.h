@@ -1,0 +1,149 @@
+/*
+ * libkaio_qkv -- GB300 (sm_103a) W4A16 fused QKV projection and dense f16
+ * tensor-core matmul behind a plain C ABI.
+ *
+ * Operations follow two docs.rs source pages of the kaio-candle crate:
+ *   "kaio-candle -- src/qkv_project_int4.rs" (qkv_project_int4 and its doc
+ *   comment: input contract, validation, output dtype), and
+ *   "kaio-candle 0.2.0 -- src/matmul_tc_async.rs" (matmul_tc_async:
+ *   f16 x f16 -> f32; MatmulTcAsyncOp::bwd: dA = grad @ B^T, dB = A^T @ grad).
+ *
+ * Conventions shared by every entry point
+ *   - All tensor pointers are DEVICE memory on the current CUDA device, owned
+ *     by the caller, dense, row-major, with no offset or stride of their own.
+ *     The library never allocates or frees them and never keeps them.
+ *   - Every tensor pointer must be 16-byte aligned (TMA and 128-bit loads).
+ *   - Calls are asynchronous on `stream` (0 = legacy default stream). The
+ *     library does not synchronise the host. Outputs are complete when the
+ *     stream reaches that point.
+ *   - Return value: KAIO_OK (0) or a kaio_status error code; on error nothing
+ *     was launched, and kaio_last_error() returns a message for the calling
+ *     thread.
+ *   - Empty problems (M == 0 or N == 0) return KAIO_OK without a launch, like
+ *     the plan launcher of "baracuda-kernels -- src/quantize/
+ *     dequantize_per_group_backward.rs" (run returns early when the element
+ *     count is zero). K == 0 is an empty sum: the outputs are set to zero.
+ *   - The library is forward-only, like the direct-call bridge it mirrors
+ *     (gradient-tracked inputs are rejected there). The matmul backward is a
+ *     separate entry point.
+ *   - Supported device: compute capability 10.3 (GB300). Anything else gives
+ *     KAIO_ERR_UNSUPPORTED_DEVICE.
+ */
+#ifndef KAIO_QKV_H_
+#define KAIO_QKV_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* kaio_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+  KAIO_OK = 0,
+  KAIO_ERR_INVALID_VALUE = 1,      /* null pointer, bad dimension, overlap, wrong device */
+  KAIO_ERR_MISALIGNED = 2,         /* a tensor pointer is not 16-byte aligned */
+  KAIO_ERR_UNSUPPORTED_DEVICE = 3, /* current device is not compute capability 10.3 */
+  KAIO_ERR_CUDA = 4,               /* a CUDA runtime call or kernel launch failed */
+  KAIO_ERR_DEVICE_TIMEOUT = 5      /* a kernel's bounded wait gave up (see kaio_device_status) */
+} kaio_status;
+
+/*
+ * W4A16 fused tri-output QKV projection.
+ * ("kaio-candle -- src/qkv_project_int4.rs", doc comment of qkv_project_int4.)
+ *
+ * For p in {q, k, v}:
+ *   out_p[m, n] = f16( sum_{k<K} x[m, k] * Wd_p[k, n] ),
+ *   Wd_p[k, n]  = RN_f16( int4(W_p[k, n]) * s_p[k / 128, n] ),
+ * accumulated in f32, rounded to f16 (nearest even) inside the kernel.
+ *
+ *   x          f16  [M, K]      activations, shared by the three projections
+ *   wq, wk, wv u32  [K/8, N]    packed INT4 weights: nibble i (bits 4i..4i+3) of
+ *                               word [r, n] is the signed two's-complement
+ *                               weight of K-row 8r+i, column n (range [-8, 7])
+ *   sq, sk, sv f16  [K/128, N]  one scale per group of 128 K-rows and column
+ *   q, k, v    f16  [M, N]      outputs; every element is written
+ *
+ * Errors (KAIO_ERR_INVALID_VALUE unless noted): a null pointer; K not a
+ * multiple of 128 (the group size is locked at 128); N not a multiple of 8;
+ * an output overlapping an input or another output; a pointer not on the
+ * current device; misaligned pointer (KAIO_ERR_MISALIGNED).
+ *
+ * Path: M <= 16 runs the weight-streaming decode kernel (split over K across
+ * all SMs; it uses a per-(device, stream) workspace that the library
+ * allocates on the first such call and keeps: make that first call outside
+ * CUDA-graph capture). M >= 17 runs the tcgen05 tensor-core kernel.
+ */
+int kaio_qkv_project_int4(const void* x, const uint32_t* wq, const uint32_t* wk,
+                          const uint32_t* wv, const void* sq, const void* sk, const void* sv,
+                          void* q, void* k, void* v, uint32_t M, uint32_t N, uint32_t K,
+                          kaio_stream_t stream);
+
+/*
+ * Dense tensor-core matmul C = A @ B.
+ * ("kaio-candle 0.2.0 -- src/matmul_tc_async.rs", module doc and
+ * MatmulTcAsyncOp::cuda_fwd: f16 x f16 -> f32, inner dimensions must match.)
+ *
+ *   a  f16 [M, K],  b  f16 [K, N],  c  f32 [M, N] (output, every element written)
+ *
+ * Errors: null pointer; K or N not a multiple of 8 (16-byte row strides);
+ * c overlapping a or b; pointer not on the current device; misalignment.
+ */
+int kaio_matmul_tc(const void* a, const void* b, float* c, uint32_t M, uint32_t N, uint32_t K,
+                   kaio_stream_t stream);
+
+/*
+ * Backward of C = A @ B for an upstream gradient G = dL/dC.
+ * ("kaio-candle 0.2.0 -- src/matmul_tc_async.rs", MatmulTcAsyncOp::bwd:
+ * dA = grad @ B^T, dB = A^T @ grad.)
+ *
+ *   a  f16 [M, K],  b  f16 [K, N],  g  f16 [M, N]
+ *   da f32 [M, K]  = G @ B^T      (output)
+ *   db f32 [K, N]  = A^T @ G      (output)
+ *
+ * The transposes are never materialised: the kernels read B and A in the
+ * other major order. The page's bridge casts grad to f16 before and the
+ * results to f16 after; here g is f16 on entry and da/db are f32 (cast them
+ * if an f16 result is wanted).
+ * Errors: as kaio_matmul_tc (K and N multiples of 8), and any output
+ * overlapping an input or the other output.
+ */
+int kaio_matmul_tc_backward(const void* a, const void* b, const void* g, float* da, float* db,
+                            uint32_t M, uint32_t N, uint32_t K, kaio_stream_t stream);
+
+/*
+ * Dequantise packed INT4 weights to f16, exactly as the projection kernels do
+ * before their multiply: out[k, n] = RN_f16(int4(W[k, n]) * s[k/128, n]).
+ * A test entry for bit-exact comparison of the dequant stage.
+ *
+ *   w  u32 [K/8, N],  s  f16 [K/128, N],  out  f16 [K, N]
+ *   variant 0: the K-row-order routine of the tensor-core kernel
+ *   variant 1: the paired-nibble routine of the decode kernel
+ * Errors: as kaio_qkv_project_int4 for K and N; variant not 0 or 1.
+ */
+int kaio_dequant_int4_debug(const uint32_t* w, const void* s, void* out, uint32_t K, uint32_t N,
+                            int variant, kaio_stream_t stream);
+
+/* Which kernel kaio_qkv_project_int4 uses for a given M: 0 = decode
+ * (weight-streaming, M <= 16), 1 = tcgen05 tensor-core kernel. */
+int kaio_qkv_path(uint32_t M);
+
+/* Message describing the last error returned on the calling thread ("" if
+ * none). The pointer stays valid until the thread's next call. */
+const char* kaio_last_error(void);
+
+/* Synchronises the current device, then reads and clears the kernels' device
+ * error word. Returns KAIO_OK, KAIO_ERR_DEVICE_TIMEOUT if a kernel gave up a
+ * bounded wait since the last query, or KAIO_ERR_CUDA if the device reports
+ * an error. */
+int kaio_device_status(void);
+
+/* Static, human-readable name of a kaio_status value. */
+const char* kaio_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KAIO_QKV_H_ */

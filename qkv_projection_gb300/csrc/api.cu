@@ -1,0 +1,386 @@
+// C ABI of libkaio_qkv: argument validation, device checks, workspace for the
+// split-K decode path, and dispatch to the kernels. No computation happens on
+// the host: every output element is produced by a kernel on the device.
+//
+// The validation mirrors the input contract of the direct-call bridge on
+// "kaio-candle -- src/qkv_project_int4.rs" (qkv_project_int4: K a multiple of
+// the locked group size 128, packed rows K/8, scale rows K/128, one N shared by
+// the six weight/scale tensors, all inputs on the one device, dimensions
+// within u32) and of MatmulTcAsyncOp::cuda_fwd on
+// "kaio-candle 0.2.0 -- src/matmul_tc_async.rs" (inner dimensions match, no CPU
+// fallback). Shapes are implied here by (M, N, K), so a row-count mismatch
+// cannot be expressed; what remains checkable is checked.
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <map>
+#include <mutex>
+#include <string>
+#include <utility>
+
+#include "../../include/kaio_qkv.h"
+#include "kaio_internal.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+int fail(int status, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return status;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(KAIO_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+struct DeviceInfo {
+  int major = 0, minor = 0, sms = 0;
+  bool ok = false;
+};
+
+std::mutex g_mu;
+std::map<int, DeviceInfo> g_devices;
+
+// Current device; fills `info` (cached). Returns KAIO_OK or an error status.
+int current_device(int* dev, DeviceInfo* info) {
+  cudaError_t e = cudaGetDevice(dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  std::lock_guard<std::mutex> lk(g_mu);
+  auto it = g_devices.find(*dev);
+  if (it == g_devices.end()) {
+    DeviceInfo d;
+    if ((e = cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, *dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, *dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, *dev)) != cudaSuccess)
+      return cuda_fail(e, "cudaDeviceGetAttribute");
+    d.ok = (d.major == 10 && d.minor == 3);
+    it = g_devices.emplace(*dev, d).first;
+  }
+  *info = it->second;
+  if (!info->ok)
+    return fail(KAIO_ERR_UNSUPPORTED_DEVICE,
+                "device %d has compute capability %d.%d; this library is built for sm_103a "
+                "(compute capability 10.3, GB300) only",
+                *dev, info->major, info->minor);
+  return KAIO_OK;
+}
+
+struct Span {
+  const char* name;
+  const void* p;
+  size_t bytes;
+};
+
+int check_not_null(const Span* s, int n) {
+  for (int i = 0; i < n; ++i)
+    if (s[i].p == nullptr) return fail(KAIO_ERR_INVALID_VALUE, "%s is a null pointer", s[i].name);
+  return KAIO_OK;
+}
+
+int check_aligned(const Span* s, int n) {
+  for (int i = 0; i < n; ++i)
+    if (reinterpret_cast<uintptr_t>(s[i].p) % 16 != 0)
+      return fail(KAIO_ERR_MISALIGNED, "%s (%p) is not 16-byte aligned", s[i].name, s[i].p);
+  return KAIO_OK;
+}
+
+bool overlaps(const Span& a, const Span& b) {
+  if (a.bytes == 0 || b.bytes == 0) return false;
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a.p), b0 = reinterpret_cast<uintptr_t>(b.p);
+  return a0 < b0 + b.bytes && b0 < a0 + a.bytes;
+}
+
+// Every output must be disjoint from every input and from the other outputs.
+int check_overlap(const Span* in, int n_in, const Span* out, int n_out) {
+  for (int i = 0; i < n_out; ++i) {
+    for (int j = 0; j < n_in; ++j)
+      if (overlaps(out[i], in[j]))
+        return fail(KAIO_ERR_INVALID_VALUE, "output %s overlaps input %s", out[i].name, in[j].name);
+    for (int j = i + 1; j < n_out; ++j)
+      if (overlaps(out[i], out[j]))
+        return fail(KAIO_ERR_INVALID_VALUE, "outputs %s and %s overlap", out[i].name, out[j].name);
+  }
+  return KAIO_OK;
+}
+
+// Each pointer must be device (or managed) memory of the current device.
+int check_on_device(const Span* s, int n, int dev) {
+  for (int i = 0; i < n; ++i) {
+    cudaPointerAttributes a{};
+    cudaError_t e = cudaPointerGetAttributes(&a, s[i].p);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return fail(KAIO_ERR_INVALID_VALUE, "%s (%p) is not CUDA device memory (%s)", s[i].name,
+                  s[i].p, cudaGetErrorName(e));
+    }
+    if (a.type != cudaMemoryTypeDevice && a.type != cudaMemoryTypeManaged)
+      return fail(KAIO_ERR_INVALID_VALUE, "%s (%p) is not device memory (memory type %d)",
+                  s[i].name, s[i].p, static_cast<int>(a.type));
+    if (a.device != dev)
+      return fail(KAIO_ERR_INVALID_VALUE, "%s is on device %d but the current device is %d",
+                  s[i].name, a.device, dev);
+  }
+  return KAIO_OK;
+}
+
+// ------------------------------------------------- decode split-K workspace
+struct Workspace {
+  void* ptr = nullptr;
+  size_t counter_cap = 0;   // number of u32 counters at the front (kept zero)
+  size_t partial_cap = 0;   // floats after the counters
+};
+std::map<std::pair<int, cudaStream_t>, Workspace> g_ws;
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+int get_workspace(int dev, cudaStream_t stream, size_t counters, size_t partial_floats,
+                  unsigned** counters_out, float** partials_out) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  Workspace& w = g_ws[{dev, stream}];
+  if (w.ptr == nullptr || counters > w.counter_cap || partial_floats > w.partial_cap) {
+    const size_t ccap = std::max(counters, w.counter_cap);
+    const size_t pcap = std::max(partial_floats, w.partial_cap);
+    if (w.ptr) {
+      // Earlier launches on this stream may still use the old buffer.
+      cudaError_t e = cudaStreamSynchronize(stream);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize (workspace growth)");
+      cudaFree(w.ptr);
+      w.ptr = nullptr;
+    }
+    const size_t cbytes = align_up(ccap * sizeof(unsigned), 256);
+    cudaError_t e = cudaMalloc(&w.ptr, cbytes + pcap * sizeof(float));
+    if (e != cudaSuccess) {
+      w = Workspace{};
+      return cuda_fail(e, "cudaMalloc (decode workspace)");
+    }
+    e = cudaMemsetAsync(w.ptr, 0, cbytes, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync (decode counters)");
+    w.counter_cap = ccap;
+    w.partial_cap = pcap;
+  }
+  *counters_out = static_cast<unsigned*>(w.ptr);
+  *partials_out = reinterpret_cast<float*>(static_cast<char*>(w.ptr) +
+                                           align_up(w.counter_cap * sizeof(unsigned), 256));
+  return KAIO_OK;
+}
+
+int zero_outputs(const Span* out, int n, cudaStream_t stream) {
+  for (int i = 0; i < n; ++i) {
+    cudaError_t e = cudaMemsetAsync(const_cast<void*>(out[i].p), 0, out[i].bytes, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync (K == 0)");
+  }
+  return KAIO_OK;
+}
+
+#define KAIO_TRY(expr)           \
+  do {                           \
+    const int st__ = (expr);     \
+    if (st__ != KAIO_OK) return st__; \
+  } while (0)
+
+}  // namespace
+
+extern "C" {
+
+const char* kaio_last_error(void) { return g_last_error.c_str(); }
+
+const char* kaio_status_string(int status) {
+  switch (status) {
+    case KAIO_OK: return "KAIO_OK";
+    case KAIO_ERR_INVALID_VALUE: return "KAIO_ERR_INVALID_VALUE";
+    case KAIO_ERR_MISALIGNED: return "KAIO_ERR_MISALIGNED";
+    case KAIO_ERR_UNSUPPORTED_DEVICE: return "KAIO_ERR_UNSUPPORTED_DEVICE";
+    case KAIO_ERR_CUDA: return "KAIO_ERR_CUDA";
+    case KAIO_ERR_DEVICE_TIMEOUT: return "KAIO_ERR_DEVICE_TIMEOUT";
+    default: return "unknown kaio_status";
+  }
+}
+
+int kaio_qkv_path(uint32_t M) { return M <= 16 ? 0 : 1; }
+
+int kaio_qkv_project_int4(const void* x, const uint32_t* wq, const uint32_t* wk, const uint32_t* wv,
+                          const void* sq, const void* sk, const void* sv, void* q, void* k, void* v,
+                          uint32_t M, uint32_t N, uint32_t K, kaio_stream_t stream_) {
+  g_last_error.clear();
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  const size_t m = M, n = N, kk = K;
+  const Span in[7] = {{"x", x, m * kk * 2},          {"w_q_packed", wq, kk / 8 * n * 4},
+                      {"w_k_packed", wk, kk / 8 * n * 4}, {"w_v_packed", wv, kk / 8 * n * 4},
+                      {"scales_q", sq, kk / 128 * n * 2}, {"scales_k", sk, kk / 128 * n * 2},
+                      {"scales_v", sv, kk / 128 * n * 2}};
+  const Span out[3] = {{"q", q, m * n * 2}, {"k", k, m * n * 2}, {"v", v, m * n * 2}};
+  KAIO_TRY(check_not_null(in, 7));
+  KAIO_TRY(check_not_null(out, 3));
+  if (K % 128 != 0)
+    return fail(KAIO_ERR_INVALID_VALUE, "K (%u) must be a multiple of group_size (128)", K);
+  if (N % 8 != 0)
+    return fail(KAIO_ERR_INVALID_VALUE, "N (%u) must be a multiple of 8 (16-byte rows)", N);
+  KAIO_TRY(check_aligned(in, 7));
+  KAIO_TRY(check_aligned(out, 3));
+  if (static_cast<uint64_t>(K) / 8 * N > 0x7FFFFFFFull || static_cast<uint64_t>(M) * K > (1ull << 40))
+    return fail(KAIO_ERR_INVALID_VALUE, "problem too large (M=%u N=%u K=%u)", M, N, K);
+  KAIO_TRY(check_overlap(in, 7, out, 3));
+  int dev;
+  DeviceInfo info;
+  KAIO_TRY(current_device(&dev, &info));
+  if (M == 0 || N == 0) return KAIO_OK;
+  KAIO_TRY(check_on_device(out, 3, dev));
+  if (K == 0) return zero_outputs(out, 3, stream);
+  KAIO_TRY(check_on_device(in, 7, dev));
+
+  const uint32_t* w3[3] = {wq, wk, wv};
+  const __half* s3[3] = {static_cast<const __half*>(sq), static_cast<const __half*>(sk),
+                         static_cast<const __half*>(sv)};
+  __half* o3[3] = {static_cast<__half*>(q), static_cast<__half*>(k), static_cast<__half*>(v)};
+
+  cudaError_t e;
+  if (kaio_qkv_path(M) == 0) {
+    const kaio::DecodePlan pl = kaio::plan_decode(static_cast<int>(M), static_cast<int>(N),
+                                                  static_cast<int>(K), info.sms);
+    unsigned* counters = nullptr;
+    float* partials = nullptr;
+    KAIO_TRY(get_workspace(dev, stream, pl.counters, pl.partial_floats, &counters, &partials));
+    kaio::DecodeParams prm{};
+    prm.x = static_cast<const __half*>(x);
+    for (int i = 0; i < 3; ++i) {
+      prm.w[i] = w3[i];
+      prm.s[i] = s3[i];
+      prm.out[i] = o3[i];
+    }
+    prm.M = static_cast<int>(M);
+    prm.N = static_cast<int>(N);
+    prm.K = static_cast<int>(K);
+    prm.groups_per_proj = pl.groups_per_proj;
+    prm.nkb = pl.nkb;
+    prm.units = pl.units;
+    prm.ctas = pl.ctas;
+    prm.xmax_kb = pl.xmax_kb;
+    prm.partials = partials;
+    prm.counters = counters;
+    e = kaio::launch_decode(prm, pl, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
+  } else {
+    e = kaio::launch_tc_w4a16(static_cast<const __half*>(x), w3, s3, o3, static_cast<int>(M),
+                              static_cast<int>(N), static_cast<int>(K), info.sms, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "tcgen05 W4A16 kernel launch");
+  }
+  return KAIO_OK;
+}
+
+int kaio_matmul_tc(const void* a, const void* b, float* c, uint32_t M, uint32_t N, uint32_t K,
+                   kaio_stream_t stream_) {
+  g_last_error.clear();
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  const size_t m = M, n = N, kk = K;
+  const Span in[2] = {{"a", a, m * kk * 2}, {"b", b, kk * n * 2}};
+  const Span out[1] = {{"c", c, m * n * 4}};
+  KAIO_TRY(check_not_null(in, 2));
+  KAIO_TRY(check_not_null(out, 1));
+  if (K % 8 != 0 || N % 8 != 0)
+    return fail(KAIO_ERR_INVALID_VALUE, "K (%u) and N (%u) must be multiples of 8 (16-byte rows)", K, N);
+  KAIO_TRY(check_aligned(in, 2));
+  KAIO_TRY(check_aligned(out, 1));
+  KAIO_TRY(check_overlap(in, 2, out, 1));
+  int dev;
+  DeviceInfo info;
+  KAIO_TRY(current_device(&dev, &info));
+  if (M == 0 || N == 0) return KAIO_OK;
+  if (K == 0) {
+    KAIO_TRY(check_on_device(out, 1, dev));
+    return zero_outputs(out, 1, stream);
+  }
+  KAIO_TRY(check_on_device(in, 2, dev));
+  KAIO_TRY(check_on_device(out, 1, dev));
+  cudaError_t e = kaio::launch_tc_gemm(a, b, c, {static_cast<int>(M), static_cast<int>(N), static_cast<int>(K)},
+                                       /*a_mn=*/false, /*b_mn=*/true, info.sms, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "tcgen05 matmul launch");
+  return KAIO_OK;
+}
+
+int kaio_matmul_tc_backward(const void* a, const void* b, const void* g, float* da, float* db,
+                            uint32_t M, uint32_t N, uint32_t K, kaio_stream_t stream_) {
+  g_last_error.clear();
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  const size_t m = M, n = N, kk = K;
+  const Span in[3] = {{"a", a, m * kk * 2}, {"b", b, kk * n * 2}, {"g", g, m * n * 2}};
+  const Span out[2] = {{"da", da, m * kk * 4}, {"db", db, kk * n * 4}};
+  KAIO_TRY(check_not_null(in, 3));
+  KAIO_TRY(check_not_null(out, 2));
+  if (K % 8 != 0 || N % 8 != 0)
+    return fail(KAIO_ERR_INVALID_VALUE, "K (%u) and N (%u) must be multiples of 8 (16-byte rows)", K, N);
+  KAIO_TRY(check_aligned(in, 3));
+  KAIO_TRY(check_aligned(out, 2));
+  KAIO_TRY(check_overlap(in, 3, out, 2));
+  int dev;
+  DeviceInfo info;
+  KAIO_TRY(current_device(&dev, &info));
+  if (K == 0) return KAIO_OK;                      // dA [M,0] and dB [0,N] are empty
+  if (M == 0 || N == 0) {
+    // Empty contraction for the non-empty output: it is all zeros.
+    KAIO_TRY(check_on_device(out, 2, dev));
+    return zero_outputs(out, 2, stream);
+  }
+  KAIO_TRY(check_on_device(in, 3, dev));
+  KAIO_TRY(check_on_device(out, 2, dev));
+  // dA[M, K] = G[M, N] @ B^T: Aop = G stored [M][N] (K-major over N);
+  //   Bop = B^T, an N x K operand whose storage B[K][N] is [No][Ko] (K-major).
+  cudaError_t e = kaio::launch_tc_gemm(g, b, da, {static_cast<int>(M), static_cast<int>(K), static_cast<int>(N)},
+                                       false, false, info.sms, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "tcgen05 matmul launch (dA)");
+  // dB[K, N] = A^T @ G: Aop = A^T, a K x M operand stored A[M][K] = [Ko][Mo]
+  //   (MN-major); Bop = G, M x N stored [Ko][No] (MN-major).
+  e = kaio::launch_tc_gemm(a, g, db, {static_cast<int>(K), static_cast<int>(N), static_cast<int>(M)},
+                           true, true, info.sms, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "tcgen05 matmul launch (dB)");
+  return KAIO_OK;
+}
+
+int kaio_dequant_int4_debug(const uint32_t* w, const void* s, void* out, uint32_t K, uint32_t N,
+                            int variant, kaio_stream_t stream_) {
+  g_last_error.clear();
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  const size_t n = N, kk = K;
+  const Span in[2] = {{"w", w, kk / 8 * n * 4}, {"s", s, kk / 128 * n * 2}};
+  const Span o[1] = {{"out", out, kk * n * 2}};
+  KAIO_TRY(check_not_null(in, 2));
+  KAIO_TRY(check_not_null(o, 1));
+  if (K % 128 != 0)
+    return fail(KAIO_ERR_INVALID_VALUE, "K (%u) must be a multiple of group_size (128)", K);
+  if (N % 8 != 0) return fail(KAIO_ERR_INVALID_VALUE, "N (%u) must be a multiple of 8", N);
+  if (variant != 0 && variant != 1)
+    return fail(KAIO_ERR_INVALID_VALUE, "variant (%d) must be 0 or 1", variant);
+  KAIO_TRY(check_aligned(in, 2));
+  KAIO_TRY(check_aligned(o, 1));
+  KAIO_TRY(check_overlap(in, 2, o, 1));
+  int dev;
+  DeviceInfo info;
+  KAIO_TRY(current_device(&dev, &info));
+  if (K == 0 || N == 0) return KAIO_OK;
+  KAIO_TRY(check_on_device(in, 2, dev));
+  KAIO_TRY(check_on_device(o, 1, dev));
+  cudaError_t e = kaio::launch_dequant_debug(w, static_cast<const __half*>(s),
+                                             static_cast<__half*>(out), static_cast<int>(K),
+                                             static_cast<int>(N), variant, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "dequant kernel launch");
+  return KAIO_OK;
+}
+
+int kaio_device_status(void) {
+  g_last_error.clear();
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+  const unsigned err = kaio::read_and_clear_tc_errors();
+  if (err == 0xFFFFFFFFu) return fail(KAIO_ERR_CUDA, "could not read the device error word");
+  if (err & kaio::kDevErrTimeoutHost)
+    return fail(KAIO_ERR_DEVICE_TIMEOUT, "a kernel gave up a bounded wait (device error word 0x%x)", err);
+  return KAIO_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,80 @@
+// Internal (non-exported) declarations shared by the translation units of
+// libkaio_qkv: kernel parameter blocks, launch plans and launchers.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstddef>
+#include <cstdint>
+
+namespace kaio {
+
+// ---------------------------------------------------------------- decode path
+struct DecodeParams {
+  const __half* x;          // [M, K]
+  const uint32_t* w[3];     // [K/8, N] each
+  const __half* s[3];       // [K/128, N] each
+  __half* out[3];           // [M, N] each
+  int M, N, K;
+  int groups_per_proj;      // ceil(N / 256)
+  int nkb;                  // K / 64
+  long long units;          // 3 * groups_per_proj * nkb
+  int ctas;                 // grid size
+  int xmax_kb;              // k-blocks of x staged in shared memory at once
+  float* partials;          // [ctas][2][8][32][8*mt] split-K partial sums
+  unsigned* counters;       // [3 * groups_per_proj], zero between launches
+};
+
+struct DecodePlan {
+  int mt;                   // 1: M <= 8, 2: M <= 16
+  int groups_per_proj;
+  int nkb;
+  long long units;
+  int ctas;
+  int xmax_kb;
+  size_t smem;
+  size_t partial_floats;
+  int counters;
+};
+
+DecodePlan plan_decode(int M, int N, int K, int num_sms);
+cudaError_t launch_decode(const DecodeParams& prm, const DecodePlan& pl, cudaStream_t stream);
+
+// ------------------------------------------------- tensor-core (tcgen05) paths
+struct GemmShape {
+  int M, N, K;              // C[M, N] = sum_k Aop[M, k] * Bop[k, N]
+};
+
+// Dense f16 x f16 -> f32. a_mn / b_mn select the operand storage:
+//   Aop K-major: A stored [M][K];  MN-major: A stored [K][M]
+//   Bop K-major: B stored [N][K];  MN-major: B stored [K][N]
+cudaError_t launch_tc_gemm(const void* a, const void* b, float* c, GemmShape sh, bool a_mn,
+                           bool b_mn, int num_sms, cudaStream_t stream);
+
+// W4A16 fused projection for M >= 17 on tcgen05 (weights as the TMEM operand).
+cudaError_t launch_tc_w4a16(const __half* x, const uint32_t* const w[3], const __half* const s[3],
+                            __half* const out[3], int M, int N, int K, int num_sms,
+                            cudaStream_t stream);
+
+// Bit-exact dequantisation (debug / test entry).
+cudaError_t launch_dequant_debug(const uint32_t* w, const __half* s, __half* out, int K, int N,
+                                 int variant, cudaStream_t stream);
+
+// Device error word (bounded-wait timeouts), read and cleared by the host API.
+constexpr unsigned kDevErrTimeoutHost = 1u;   // same bit as kDevErrTimeout in kaio_device.cuh
+unsigned read_and_clear_tc_errors();
+
+// Raise a kernel's dynamic shared memory limit once per (kernel, device):
+// later calls (including those made while a stream is being captured into a
+// CUDA graph) only look the pair up.
+cudaError_t ensure_smem_limit(const void* kernel, int bytes);
+
+// Driver entry point for tensor-map encoding (resolved once through the runtime).
+CUresult encode_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
+                              uint64_t inner, uint64_t outer, uint64_t row_bytes,
+                              uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swz);
+
+}  // namespace kaio

@@ -1,0 +1,611 @@
+// tcgen05 (5th-generation tensor core) kernels of libkaio_qkv:
+//
+//  * tc_gemm_kernel: dense f16 x f16 -> f32, C = Aop * Bop, for
+//    "kaio-candle 0.2.0 -- src/matmul_tc_async.rs" (forward, and the backward
+//    dA = grad * B^T, dB = A^T * grad of MatmulTcAsyncOp::bwd, taken here by
+//    reading the stored operands in the other major order instead of copying
+//    transposes).
+//  * tc_w4a16_kernel: the W4A16 fused QKV projection of
+//    "kaio-candle -- src/qkv_project_int4.rs" for M >= 17.
+//
+// Both share one pipeline shape: a TMA producer warp fills a ring of shared
+// memory stages, a single thread issues tcgen05.mma into f32 accumulators in
+// tensor memory, and the remaining warps drain the accumulators with
+// tcgen05.ld and write the outputs. Every wait on an mbarrier is bounded.
+//
+// Dense: A and B both come from shared memory (128B-swizzled TMA tiles);
+// 128 x 256 output tile; two accumulator buffers so the epilogue of one tile
+// overlaps the main loop of the next.
+//
+// W4A16: the product is computed transposed, D_p[n, m] = Wd_p^T[n, :] x^T[:, m],
+// so that the dequantised weights are the MMA's A operand and can live in
+// tensor memory: eight dequant warps read packed words from the staged tile,
+// build f16 operands in registers and write them to TMEM with tcgen05.st; the
+// shared activation tile x is the B operand and is read once per k-step for all
+// three projections. No dequantised weight ever touches shared memory.
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+#include <set>
+#include <tuple>
+
+#include "kaio_device.cuh"
+#include "kaio_internal.h"
+
+namespace kaio {
+
+__device__ unsigned g_tc_err = 0;
+
+namespace {
+
+// ============================================================== dense GEMM
+constexpr int GBM = 128, GBN = 256, GBK = 64, GSTAGES = 4;
+constexpr int GA_BYTES = GBM * GBK * 2;        // 16 KB
+constexpr int GB_BYTES = GBN * GBK * 2;        // 32 KB
+constexpr int GSTAGE_BYTES = GA_BYTES + GB_BYTES;
+constexpr int GTHREADS = 192;                  // w0 TMA, w1 MMA, w2..5 epilogue
+constexpr uint32_t GTMEM_COLS = 512;           // 2 x 256 f32 accumulators
+constexpr size_t GSMEM = static_cast<size_t>(GSTAGES) * GSTAGE_BYTES + 1024;
+
+struct GemmParams {
+  float* c;
+  int M, N, K;
+  int m_blocks, tiles;
+};
+
+template <bool A_MN, bool B_MN>
+__global__ void __launch_bounds__(GTHREADS, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const GemmParams p) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  __shared__ __align__(8) uint64_t full[GSTAGES], empty[GSTAGES], acc_full[2], acc_empty[2],
+      mma_done;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_flag;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < GSTAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 4);
+    }
+    mbar_init(&mma_done, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_base_sh, GTMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+  const int nk = (p.K + GBK - 1) / GBK;
+  volatile int* abort = &abort_flag;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      tma_prefetch_desc(&tmA);
+      tma_prefetch_desc(&tmB);
+      int st = 0;
+      uint32_t ph = 0;
+      uint32_t fills[GSTAGES] = {0, 0, 0, 0};
+      for (int tile = blockIdx.x; tile < p.tiles; tile += gridDim.x) {
+        const int m0 = (tile % p.m_blocks) * GBM, n0 = (tile / p.m_blocks) * GBN;
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!mbar_wait(&empty[st], ph ^ 1, abort, &g_tc_err)) goto producer_done;
+          ++fills[st];
+          unsigned char* sa = smem + st * GSTAGE_BYTES;
+          unsigned char* sb = sa + GA_BYTES;
+          mbar_arrive_expect_tx(&full[st], GSTAGE_BYTES);
+          if (!A_MN) {
+            tma_load_2d(sa, &tmA, &full[st], kb * GBK, m0);
+          } else {
+            tma_load_2d(sa, &tmA, &full[st], m0, kb * GBK);
+            tma_load_2d(sa + 8192, &tmA, &full[st], m0 + 64, kb * GBK);
+          }
+          if (!B_MN) {
+            tma_load_2d(sb, &tmB, &full[st], kb * GBK, n0);
+          } else {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) tma_load_2d(sb + q * 8192, &tmB, &full[st], n0 + 64 * q, kb * GBK);
+          }
+          if (++st == GSTAGES) { st = 0; ph ^= 1; }
+        }
+      }
+    producer_done:
+      // No copy may still be landing in shared memory when the CTA exits:
+      // wait for the last fill of every stage to complete.
+      for (int s2 = 0; s2 < GSTAGES; ++s2)
+        if (fills[s2]) mbar_wait_drain(&full[s2], (fills[s2] - 1) & 1, &g_tc_err);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_f16_f32(GBM, GBN, A_MN, B_MN);
+      int st = 0;
+      uint32_t ph = 0;
+      int buf = 0;
+      uint32_t aph = 0;
+      for (int tile = blockIdx.x; tile < p.tiles; tile += gridDim.x) {
+        if (!mbar_wait(&acc_empty[buf], aph ^ 1, abort, &g_tc_err)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + buf * GBN;
+        bool ok = true;
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!mbar_wait(&full[st], ph, abort, &g_tc_err)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + st * GSTAGE_BYTES);
+          const uint32_t sb = sa + GA_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < GBK / 16; ++kk) {
+            const uint64_t ad = A_MN ? sdesc_sw128(sa + kk * 2048, 8192, 1024)
+                                     : sdesc_sw128(sa + kk * 32, 16, 1024);
+            const uint64_t bd = B_MN ? sdesc_sw128(sb + kk * 2048, 8192, 1024)
+                                     : sdesc_sw128(sb + kk * 32, 16, 1024);
+            umma_ss(d, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+          }
+          umma_commit(&empty[st]);
+          if (++st == GSTAGES) { st = 0; ph ^= 1; }
+        }
+        if (!ok) break;
+        umma_commit(&acc_full[buf]);
+        if (++buf == 2) { buf = 0; aph ^= 1; }
+      }
+      // Every MMA issued has completed before TMEM is released.
+      umma_commit(&mma_done);
+      mbar_wait_drain(&mma_done, 0, &g_tc_err);
+    }
+  } else {
+    // Epilogue: warp w drains TMEM lanes 32*(w%4) .. +31 (rows of the tile).
+    const int sp = warp & 3;
+    int buf = 0;
+    uint32_t aph = 0;
+    for (int tile = blockIdx.x; tile < p.tiles; tile += gridDim.x) {
+      const int m0 = (tile % p.m_blocks) * GBM, n0 = (tile / p.m_blocks) * GBN;
+      if (!mbar_wait(&acc_full[buf], aph, abort, &g_tc_err)) break;
+      tc_fence_after();
+      const int row = m0 + 32 * sp + lane;
+      float* crow = p.c + static_cast<size_t>(row) * p.N;
+#pragma unroll 1
+      for (int ch = 0; ch < GBN / 32; ++ch) {
+        uint32_t r[32];
+        tmem_ld32(tmem + (static_cast<uint32_t>(32 * sp) << 16) + buf * GBN + ch * 32, r);
+        tmem_ld_wait();
+        const int col0 = n0 + ch * 32;
+        if (row < p.M) {
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const int col = col0 + 4 * q;
+            if (col < p.N)
+              *reinterpret_cast<float4*>(crow + col) =
+                  make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
+                              __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[buf]);
+      if (++buf == 2) { buf = 0; aph ^= 1; }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, GTMEM_COLS);
+  }
+}
+
+// ============================================================ W4A16 prefill
+constexpr int PBM = 128;                 // x rows per tile        (MMA N)
+constexpr int PBN = 128;                 // output columns per tile (MMA M)
+constexpr int PBK = 64;                  // K per TMA stage
+constexpr int PSTAGES = 4;
+constexpr int PX_BYTES = PBM * PBK * 2;          // 16384
+constexpr int PW_BYTES = (PBK / 8) * PBN * 4;    // 4096 per projection
+constexpr int PS_BYTES = PBN * 2;                // 256 per projection
+constexpr int PTX_BYTES = PX_BYTES + 3 * PW_BYTES + 3 * PS_BYTES;  // bytes landed per stage
+constexpr int PSTAGE_BYTES = 30720;              // padded to keep x tiles 1024-aligned
+constexpr int PTHREADS = 320;                    // w0 TMA, w1 MMA, w2..9 dequant + epilogue
+constexpr int PDQ_WARPS = 8;
+constexpr uint32_t PTMEM_COLS = 512;
+constexpr uint32_t PA_COL0 = 384;                // A stages after the three accumulators
+constexpr uint32_t PA_STAGE_COLS = 48;           // 3 projections x 16 columns (32 K)
+constexpr size_t PSMEM = static_cast<size_t>(PSTAGES) * PSTAGE_BYTES + 1024;
+static_assert(PTX_BYTES <= PSTAGE_BYTES, "stage layout");
+
+struct W4Params {
+  __half* out[3];
+  int M, N, K;
+  int m_blocks, tiles;
+};
+
+__global__ void __launch_bounds__(PTHREADS, 1)
+    tc_w4a16_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW0,
+                    const __grid_constant__ CUtensorMap tmW1, const __grid_constant__ CUtensorMap tmW2,
+                    const __grid_constant__ CUtensorMap tmS0, const __grid_constant__ CUtensorMap tmS1,
+                    const __grid_constant__ CUtensorMap tmS2, const W4Params p) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  __shared__ __align__(8) uint64_t full[PSTAGES], empty[PSTAGES], a_full[2], a_empty[2],
+      acc_full, acc_empty, mma_done;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_flag;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < PSTAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1 + PDQ_WARPS);  // MMA commit + every dequant warp
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&a_full[a], PDQ_WARPS);
+      mbar_init(&a_empty[a], 1);
+    }
+    mbar_init(&acc_full, 1);
+    mbar_init(&acc_empty, PDQ_WARPS);
+    mbar_init(&mma_done, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_base_sh, PTMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+  const int nks = p.K / PBK;   // K is a multiple of 128
+  volatile int* abort = &abort_flag;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      tma_prefetch_desc(&tmX);
+      tma_prefetch_desc(&tmW0); tma_prefetch_desc(&tmW1); tma_prefetch_desc(&tmW2);
+      tma_prefetch_desc(&tmS0); tma_prefetch_desc(&tmS1); tma_prefetch_desc(&tmS2);
+      int st = 0;
+      uint32_t ph = 0;
+      uint32_t fills[PSTAGES] = {0, 0, 0, 0};
+      for (int tile = blockIdx.x; tile < p.tiles; tile += gridDim.x) {
+        const int m0 = (tile % p.m_blocks) * PBM, n0 = (tile / p.m_blocks) * PBN;
+        for (int ks = 0; ks < nks; ++ks) {
+          if (!mbar_wait(&empty[st], ph ^ 1, abort, &g_tc_err)) goto producer_done;
+          ++fills[st];
+          unsigned char* sx = smem + st * PSTAGE_BYTES;
+          mbar_arrive_expect_tx(&full[st], PTX_BYTES);
+          tma_load_2d(sx, &tmX, &full[st], ks * PBK, m0);
+          unsigned char* sw = sx + PX_BYTES;
+          unsigned char* ss = sx + PX_BYTES + 3 * PW_BYTES;
+          tma_load_2d(sw, &tmW0, &full[st], n0, ks * (PBK / 8));
+          tma_load_2d(sw + PW_BYTES, &tmW1, &full[st], n0, ks * (PBK / 8));
+          tma_load_2d(sw + 2 * PW_BYTES, &tmW2, &full[st], n0, ks * (PBK / 8));
+          tma_load_2d(ss, &tmS0, &full[st], n0, ks >> 1);
+          tma_load_2d(ss + PS_BYTES, &tmS1, &full[st], n0, ks >> 1);
+          tma_load_2d(ss + 2 * PS_BYTES, &tmS2, &full[st], n0, ks >> 1);
+          if (++st == PSTAGES) { st = 0; ph ^= 1; }
+        }
+      }
+    producer_done:
+      for (int s2 = 0; s2 < PSTAGES; ++s2)
+        if (fills[s2]) mbar_wait_drain(&full[s2], (fills[s2] - 1) & 1, &g_tc_err);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_f16_f32(PBN, PBM, false, false);
+      int st = 0, a = 0;
+      uint32_t ph = 0, aph = 0, cph = 0;
+      for (int tile = blockIdx.x; tile < p.tiles; tile += gridDim.x) {
+        if (!mbar_wait(&acc_empty, cph ^ 1, abort, &g_tc_err)) break;
+        tc_fence_after();
+        bool ok = true;
+        for (int ks = 0; ks < nks && ok; ++ks) {
+          if (!mbar_wait(&full[st], ph, abort, &g_tc_err)) { ok = false; break; }
+          const uint32_t sx = smem_u32(smem + st * PSTAGE_BYTES);
+          for (int hh = 0; hh < 2; ++hh) {
+            if (!mbar_wait(&a_full[a], aph, abort, &g_tc_err)) { ok = false; break; }
+            tc_fence_after();
+#pragma unroll
+            for (int q = 0; q < 3; ++q) {
+#pragma unroll
+              for (int kk = 0; kk < 2; ++kk) {
+                const uint32_t at = tmem + PA_COL0 + a * PA_STAGE_COLS + q * 16 + kk * 8;
+                const uint64_t bd = sdesc_sw128(sx + (2 * hh + kk) * 32, 16, 1024);
+                umma_ts(tmem + q * PBM, at, bd, idesc, (ks | hh | kk) != 0 ? 1u : 0u);
+              }
+            }
+            umma_commit(&a_empty[a]);
+            if (++a == 2) { a = 0; aph ^= 1; }
+          }
+          if (!ok) break;
+          umma_commit(&empty[st]);
+          if (++st == PSTAGES) { st = 0; ph ^= 1; }
+        }
+        if (!ok) break;
+        umma_commit(&acc_full);
+        cph ^= 1;
+      }
+      umma_commit(&mma_done);
+      mbar_wait_drain(&mma_done, 0, &g_tc_err);
+    }
+  } else {
+    // Dequant + epilogue warps. TMEM lane group sp = warp % 4: this thread owns
+    // output column n0 + 32*sp + lane (TMEM lane = A row = column). hf picks the
+    // two packed rows (16 K) of each 32-K A stage this warp fills, and the half
+    // of the x rows it drains in the epilogue.
+    const int sp = warp & 3;
+    const int hf = (warp - 2) >> 2;
+    const int nl = 32 * sp + lane;
+    const uint32_t lane_base = static_cast<uint32_t>(32 * sp) << 16;
+    int st = 0, a = 0;
+    uint32_t ph = 0, aph = 0, cph = 0;
+    for (int tile = blockIdx.x; tile < p.tiles; tile += gridDim.x) {
+      const int m0 = (tile % p.m_blocks) * PBM, n0 = (tile / p.m_blocks) * PBN;
+      bool ok = true;
+      for (int ks = 0; ks < nks && ok; ++ks) {
+        if (!mbar_wait(&full[st], ph, abort, &g_tc_err)) { ok = false; break; }
+        const unsigned char* sx = smem + st * PSTAGE_BYTES;
+        const uint32_t* sw = reinterpret_cast<const uint32_t*>(sx + PX_BYTES);
+        const __half* ss = reinterpret_cast<const __half*>(sx + PX_BYTES + 3 * PW_BYTES);
+        uint32_t s2[3];
+#pragma unroll
+        for (int q = 0; q < 3; ++q) {
+          const uint16_t sb = __half_as_ushort(ss[q * PBN + nl]);
+          s2[q] = half2_bits(sb, sb);
+        }
+        for (int hh = 0; hh < 2; ++hh) {
+          if (!mbar_wait(&a_empty[a], aph ^ 1, abort, &g_tc_err)) { ok = false; break; }
+          tc_fence_after();
+          const int r0 = hh * 4 + hf * 2;
+#pragma unroll
+          for (int q = 0; q < 3; ++q) {
+            const uint32_t w0 = sw[q * (PW_BYTES / 4) + r0 * PBN + nl];
+            const uint32_t w1 = sw[q * (PW_BYTES / 4) + (r0 + 1) * PBN + nl];
+            uint32_t v0[4], v1[4];
+            dequant_natural(w0, s2[q], v0);
+            dequant_natural(w1, s2[q], v1);
+            const uint32_t v[8] = {v0[0], v0[1], v0[2], v0[3], v1[0], v1[1], v1[2], v1[3]};
+            tmem_st8(tmem + lane_base + PA_COL0 + a * PA_STAGE_COLS + q * 16 + hf * 8, v);
+          }
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&a_full[a]);
+          if (++a == 2) { a = 0; aph ^= 1; }
+        }
+        if (!ok) break;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[st]);
+        if (++st == PSTAGES) { st = 0; ph ^= 1; }
+      }
+      if (!ok) break;
+
+      // Epilogue: D_q[n][m] -> out_q[m0 + m][n0 + n] as f16.
+      if (!mbar_wait(&acc_full, cph, abort, &g_tc_err)) break;
+      tc_fence_after();
+      const int n = n0 + nl;
+      const bool odd = lane & 1;
+      const int ncol = n0 + (nl & ~1);
+#pragma unroll 1
+      for (int q = 0; q < 3; ++q) {
+        __half* out = (q == 0) ? p.out[0] : (q == 1) ? p.out[1] : p.out[2];
+#pragma unroll 1
+        for (int mh = 0; mh < 2; ++mh) {
+          const int mb = 64 * hf + 32 * mh;
+          uint32_t r[32];
+          tmem_ld32(tmem + lane_base + q * PBM + mb, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 32; j += 2) {
+            const float own_lo = __uint_as_float(r[j]), own_hi = __uint_as_float(r[j + 1]);
+            const float send = odd ? own_lo : own_hi;
+            const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
+            const int m = m0 + mb + j + (odd ? 1 : 0);
+            const __half2 h = odd ? __floats2half2_rn(recv, own_hi) : __floats2half2_rn(own_lo, recv);
+            if (m < p.M && ncol < p.N)
+              *reinterpret_cast<__half2*>(out + static_cast<size_t>(m) * p.N + ncol) = h;
+          }
+        }
+      }
+      (void)n;
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty);
+      cph ^= 1;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, PTMEM_COLS);
+  }
+}
+
+// ============================================================ debug dequant
+__global__ void dequant_debug_kernel(const uint32_t* __restrict__ w, const __half* __restrict__ s,
+                                     __half* __restrict__ out, int K, int N, int variant) {
+  const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const long long total = static_cast<long long>(K / 8) * N;
+  if (idx >= total) return;
+  const int r = static_cast<int>(idx / N), n = static_cast<int>(idx % N);
+  const uint32_t word = w[idx];
+  const uint16_t sb = __half_as_ushort(s[static_cast<size_t>(r / 16) * N + n]);
+  const uint32_t s2 = half2_bits(sb, sb);
+  uint16_t vals[8];
+  if (variant == 0) {
+    uint32_t o[4];
+    dequant_natural(word, s2, o);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      vals[2 * c] = static_cast<uint16_t>(o[c] & 0xFFFFu);
+      vals[2 * c + 1] = static_cast<uint16_t>(o[c] >> 16);
+    }
+  } else {
+    const PairedNibbles pn(word);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t v = pn.pair(j, s2);
+      vals[j] = static_cast<uint16_t>(v & 0xFFFFu);
+      vals[j + 4] = static_cast<uint16_t>(v >> 16);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    out[static_cast<size_t>(8 * r + i) * N + n] = __ushort_as_half(vals[i]);
+}
+
+}  // namespace
+
+// ================================================================== host side
+CUresult encode_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
+                              uint64_t inner, uint64_t outer, uint64_t row_bytes,
+                              uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swz) {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  if (!fn) return CUDA_ERROR_NOT_FOUND;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+cudaError_t ensure_smem_limit(const void* kernel, int bytes) {
+  static std::mutex mu;
+  static std::set<std::tuple<const void*, int, int>> done;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lk(mu);
+  const auto key = std::make_tuple(kernel, dev, bytes);
+  if (done.count(key)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done.insert(key);
+  return e;
+}
+
+static cudaError_t map_error(CUresult r) {
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+cudaError_t launch_tc_gemm(const void* a, const void* b, float* c, GemmShape sh, bool a_mn,
+                           bool b_mn, int num_sms, cudaStream_t stream) {
+  CUtensorMap ta, tb;
+  CUresult r;
+  // Aop is [M x K]; stored [M][K] (K-major) or [K][M] (MN-major).
+  if (!a_mn)
+    r = encode_tensor_map_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a, sh.K, sh.M,
+                             static_cast<uint64_t>(sh.K) * 2, GBK, GBM, CU_TENSOR_MAP_SWIZZLE_128B);
+  else
+    r = encode_tensor_map_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a, sh.M, sh.K,
+                             static_cast<uint64_t>(sh.M) * 2, 64, GBK, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (r != CUDA_SUCCESS) return map_error(r);
+  // Bop is [K x N]; stored [N][K] (K-major) or [K][N] (MN-major).
+  if (!b_mn)
+    r = encode_tensor_map_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, b, sh.K, sh.N,
+                             static_cast<uint64_t>(sh.K) * 2, GBK, GBN, CU_TENSOR_MAP_SWIZZLE_128B);
+  else
+    r = encode_tensor_map_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, b, sh.N, sh.K,
+                             static_cast<uint64_t>(sh.N) * 2, 64, GBK, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (r != CUDA_SUCCESS) return map_error(r);
+
+  GemmParams p{};
+  p.c = c;
+  p.M = sh.M;
+  p.N = sh.N;
+  p.K = sh.K;
+  p.m_blocks = (sh.M + GBM - 1) / GBM;
+  const int n_blocks = (sh.N + GBN - 1) / GBN;
+  p.tiles = p.m_blocks * n_blocks;
+  const int grid = std::min(p.tiles, num_sms);
+
+  cudaError_t e;
+#define KAIO_LAUNCH_GEMM(AM, BM_)                                                               \
+  do {                                                                                          \
+    e = ensure_smem_limit(reinterpret_cast<const void*>(tc_gemm_kernel<AM, BM_>), (int)GSMEM); \
+    if (e != cudaSuccess) return e;                                                             \
+    tc_gemm_kernel<AM, BM_><<<grid, GTHREADS, GSMEM, stream>>>(ta, tb, p);                      \
+  } while (0)
+  if (!a_mn && b_mn) KAIO_LAUNCH_GEMM(false, true);
+  else if (!a_mn && !b_mn) KAIO_LAUNCH_GEMM(false, false);
+  else if (a_mn && b_mn) KAIO_LAUNCH_GEMM(true, true);
+  else KAIO_LAUNCH_GEMM(true, false);
+#undef KAIO_LAUNCH_GEMM
+  return cudaGetLastError();
+}
+
+cudaError_t launch_tc_w4a16(const __half* x, const uint32_t* const w[3], const __half* const s[3],
+                            __half* const out[3], int M, int N, int K, int num_sms,
+                            cudaStream_t stream) {
+  CUtensorMap tx, tw[3], ts[3];
+  CUresult r = encode_tensor_map_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, x, K, M,
+                                    static_cast<uint64_t>(K) * 2, PBK, PBM,
+                                    CU_TENSOR_MAP_SWIZZLE_128B);
+  if (r != CUDA_SUCCESS) return map_error(r);
+  for (int q = 0; q < 3; ++q) {
+    r = encode_tensor_map_2d(&tw[q], CU_TENSOR_MAP_DATA_TYPE_UINT32, w[q], N, K / 8,
+                             static_cast<uint64_t>(N) * 4, PBN, PBK / 8, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (r != CUDA_SUCCESS) return map_error(r);
+    r = encode_tensor_map_2d(&ts[q], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, s[q], N, K / 128,
+                             static_cast<uint64_t>(N) * 2, PBN, 1, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (r != CUDA_SUCCESS) return map_error(r);
+  }
+  W4Params p{};
+  for (int q = 0; q < 3; ++q) p.out[q] = out[q];
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.m_blocks = (M + PBM - 1) / PBM;
+  const int n_blocks = (N + PBN - 1) / PBN;
+  p.tiles = p.m_blocks * n_blocks;
+  const int grid = std::min(p.tiles, num_sms);
+  cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(tc_w4a16_kernel),
+                                    static_cast<int>(PSMEM));
+  if (e != cudaSuccess) return e;
+  tc_w4a16_kernel<<<grid, PTHREADS, PSMEM, stream>>>(tx, tw[0], tw[1], tw[2], ts[0], ts[1], ts[2], p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dequant_debug(const uint32_t* w, const __half* s, __half* out, int K, int N,
+                                 int variant, cudaStream_t stream) {
+  const long long total = static_cast<long long>(K / 8) * N;
+  if (total == 0) return cudaSuccess;
+  const int threads = 256;
+  const long long blocks = (total + threads - 1) / threads;
+  dequant_debug_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(w, s, out, K, N, variant);
+  return cudaGetLastError();
+}
+
+unsigned read_and_clear_tc_errors() {
+  unsigned v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_tc_err, sizeof(v)) != cudaSuccess) return 0xFFFFFFFFu;
+  const unsigned zero = 0;
+  cudaMemcpyToSymbol(g_tc_err, &zero, sizeof(zero));
+  return v;
+}
+
+}  // namespace kaio

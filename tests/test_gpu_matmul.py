@@ -1,0 +1,74 @@
+"""Dense tcgen05 matmul and its backward against the CPU oracle (GPU)."""
+import numpy as np
+import pytest
+
+import oracle
+from qkv_projection_gb300 import kaio
+from qkv_projection_gb300.inputs import dense_inputs
+
+from gpu_helpers import rel_frobenius, to_dev, to_host
+
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-3
+
+
+@pytest.mark.parametrize("m,n,k", [(128, 256, 64), (1, 8, 8), (130, 264, 136), (257, 520, 1000),
+                                   (64, 64, 4096), (300, 1024, 256), (512, 512, 512)])
+def test_forward_small(m, n, k):
+    a, b, _ = dense_inputs(m, n, k, seed=m + n + k)
+    c = to_host(kaio.matmul_tc(to_dev(a), to_dev(b)))
+    assert rel_frobenius(c, oracle.matmul_ref(a, b)) <= TOL
+
+
+def test_forward_4096_sampled_rows():
+    a, b, _ = dense_inputs(4096, 4096, 4096, seed=0)
+    c = to_host(kaio.matmul_tc(to_dev(a), to_dev(b)))
+    rows = np.unique(np.concatenate([np.random.default_rng(1).choice(4096, 64, replace=False),
+                                     [0, 1, 127, 128, 4095]]))
+    assert rel_frobenius(c[rows], oracle.matmul_rows(a, b, rows)) <= TOL
+
+
+@pytest.mark.parametrize("m,n,k", [(128, 256, 64), (136, 264, 200), (520, 256, 384), (64, 8, 8)])
+def test_backward_small(m, n, k):
+    a, b, g = dense_inputs(m, n, k, seed=3 * m + n)
+    da, db = kaio.matmul_tc_backward(to_dev(a), to_dev(b), to_dev(g))
+    ra, rb = oracle.matmul_backward_ref(a, b, g)
+    assert rel_frobenius(to_host(da), ra) <= TOL
+    assert rel_frobenius(to_host(db), rb) <= TOL
+
+
+def test_backward_4096_sampled():
+    a, b, g = dense_inputs(4096, 4096, 4096, seed=0)
+    da, db = kaio.matmul_tc_backward(to_dev(a), to_dev(b), to_dev(g))
+    da, db = to_host(da), to_host(db)
+    rows = np.unique(np.concatenate([np.random.default_rng(2).choice(4096, 48, replace=False),
+                                     [0, 127, 128, 4095]]))
+    g64, b64, a64 = (np.asarray(t, dtype=np.float64) for t in (g, b, a))
+    # dA rows = G[rows] @ B^T ; dB rows = A[:, rows]^T @ G
+    ra = oracle.matmul_backward_ref(a[rows], b, g[rows])[0]
+    assert rel_frobenius(da[rows], ra) <= TOL
+    rb = a64[:, rows].T @ g64
+    assert rel_frobenius(db[rows], rb) <= TOL
+
+
+def test_backward_transpose_identities():
+    # A = I  ->  dB = A^T G = G exactly;  B = I  ->  dA = G B^T = G exactly
+    n = 256
+    _, b, g = dense_inputs(n, n, n, seed=4)
+    eye = np.eye(n, dtype=np.float16)
+    _, db = kaio.matmul_tc_backward(to_dev(eye), to_dev(b), to_dev(g))
+    assert np.array_equal(to_host(db), g.astype(np.float32))
+    da, _ = kaio.matmul_tc_backward(to_dev(b), to_dev(eye), to_dev(g))
+    assert np.array_equal(to_host(da), g.astype(np.float32))
+
+
+def test_forward_identity_exact():
+    a, _, _ = dense_inputs(200, 256, 256, seed=6)
+    eye = np.eye(256, dtype=np.float16)
+    c = to_host(kaio.matmul_tc(to_dev(a), to_dev(eye)))
+    assert np.array_equal(c, a.astype(np.float32))
+
+
+def test_no_device_timeouts_reported():
+    kaio.device_status()
