@@ -267,8 +267,9 @@ def run_kaio(args, cfg_name, ws, rank, local, dist):
     stream.synchronize()
     replays = -(-args.steps // chunk)
     steps = replays * chunk
-    for _ in range(2):
-        graph.replay()
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            graph.replay()
     stream.synchronize()
 
     barrier(dist)
@@ -278,10 +279,11 @@ def run_kaio(args, cfg_name, ws, rank, local, dist):
     with ClockSampler(local) as clk:
         time.sleep(0.3)
         w0 = time.perf_counter()
-        ev0.record(stream)
-        for _ in range(replays):
-            graph.replay()
-        ev1.record(stream)
+        with torch.cuda.stream(stream):      # replay() launches on the current stream
+            ev0.record(stream)
+            for _ in range(replays):
+                graph.replay()
+            ev1.record(stream)
         ev1.synchronize()
         clk.mark(w0, time.perf_counter() + 0.05)
         time.sleep(0.1)

@@ -27,8 +27,9 @@ def test_dequant_bit_exact_wide_scale_range(variant):
     # negative scales
     k, n = 128, 64
     rng = np.random.default_rng(1)
-    w = np.tile(np.arange(-8, 8, dtype=np.int8), (k // 16, n))[:, :n]
-    w = np.roll(w, 3, axis=1)
+    # column c holds every value -8..7 along K, rotated by c
+    w = np.tile(np.arange(-8, 8, dtype=np.int8).reshape(16, 1), (k // 16, n))
+    w = np.stack([np.roll(w[:, c], c) for c in range(n)], axis=1)
     packed = oracle.pack_int4(w)
     s = np.empty((1, n), dtype=np.float16)
     specials = np.array([0.0, -0.0, 6e-8, 1e-5, 6.1e-5, 0.5, 1.0, -1.0, 3.14, 1000.0, 8190.0,
