@@ -27,9 +27,9 @@
 #include <cuda_fp16.h>
 #include <cudaTypedefs.h>
 
+#include <map>
 #include <mutex>
-#include <set>
-#include <tuple>
+#include <utility>
 
 #include "kaio_device.cuh"
 #include "kaio_internal.h"
@@ -495,16 +495,25 @@ CUresult encode_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, const
 }
 
 cudaError_t ensure_smem_limit(const void* kernel, int bytes) {
+  // The attribute is one upper bound per (kernel, device): only ever raise it,
+  // so that a launch needing less never lowers it under an earlier, larger need.
   static std::mutex mu;
-  static std::set<std::tuple<const void*, int, int>> done;
+  static std::map<std::pair<const void*, int>, int> limit;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   std::lock_guard<std::mutex> lk(mu);
-  const auto key = std::make_tuple(kernel, dev, bytes);
-  if (done.count(key)) return cudaSuccess;
+  int& cur = limit[std::make_pair(kernel, dev)];
+  if (bytes <= cur) return cudaSuccess;
+  cudaFuncAttributes fa{};
+  e = cudaFuncGetAttributes(&fa, kernel);
+  if (e != cudaSuccess) return e;
+  if (fa.maxDynamicSharedSizeBytes >= bytes) {
+    cur = fa.maxDynamicSharedSizeBytes;
+    return cudaSuccess;
+  }
   e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (e == cudaSuccess) done.insert(key);
+  if (e == cudaSuccess) cur = bytes;
   return e;
 }
 

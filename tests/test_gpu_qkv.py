@@ -153,5 +153,12 @@ def test_host_pointer_rejected():
     assert "device memory" in kaio.last_error()
 
 
+def test_decode_shared_memory_sizes_in_any_order():
+    # Decode launches size their shared memory by K; a small launch between two
+    # large ones must not leave the kernel's limit below what the large one needs.
+    for m, n, k in [(1, 4096, 4096), (5, 264, 128), (1, 4096, 4096), (12, 256, 256), (16, 1032, 8192)]:
+        check_full(qkv_inputs(m, n, k, seed=k), f"sequence M={m} K={k}")
+
+
 def test_no_device_timeouts_reported():
     kaio.device_status()
