@@ -81,6 +81,38 @@ int kaio_qkv_project_int4(const void* x, const uint32_t* wq, const uint32_t* wk,
                           kaio_stream_t stream);
 
 /*
+ * kaio_qkv_project_int4 for decode-sized M (0..16) without any device memory
+ * allocation by the library. The pages have no counterpart of this entry: it
+ * exists for callers that cannot allocate device memory themselves or let a
+ * library do it -- engines and plugin hosts that own every byte of device
+ * memory and forbid cudaMalloc, processes whose memory is fully reserved up
+ * front, and latency-critical paths that cannot take an allocation's implicit
+ * synchronisation or failure.
+ *
+ * Same arguments, layouts, results and errors as kaio_qkv_project_int4, with
+ * these differences:
+ *   - M must be <= 16 (it runs the weight-streaming decode kernel); larger M
+ *     is rejected with KAIO_ERR_INVALID_VALUE.
+ *   - The kernel's split-K scratch (group counters and partial sums) lives in
+ *     one fixed 8 MiB array inside the library; every GPU that loads the
+ *     library holds it until the process exits. N is limited to 3*ceil(N/256)
+ *     <= 16384 column groups (N <= 1,398,016); larger N is rejected with
+ *     KAIO_ERR_INVALID_VALUE.
+ *   - All calls share that array. Calls whose kernels overlap on the GPU (for
+ *     example on two streams with no ordering between them) race on it and
+ *     produce wrong results: issue them in order on one stream. Each call
+ *     clears the counters it needs (cudaMemsetAsync on `stream`) before its
+ *     kernel.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   - It calls no cudaMalloc, cudaFree or other allocating routine.
+ */
+int kaio_qkv_project_int4_noalloc(const void* x, const uint32_t* wq, const uint32_t* wk,
+                                  const uint32_t* wv, const void* sq, const void* sk,
+                                  const void* sv, void* q, void* k, void* v, uint32_t M,
+                                  uint32_t N, uint32_t K, kaio_stream_t stream);
+
+/*
  * Dense tensor-core matmul C = A @ B.
  * ("kaio-candle 0.2.0 -- src/matmul_tc_async.rs", module doc and
  * MatmulTcAsyncOp::cuda_fwd: f16 x f16 -> f32, inner dimensions must match.)

@@ -274,6 +274,62 @@ int kaio_qkv_project_int4(const void* x, const uint32_t* wq, const uint32_t* wk,
   return KAIO_OK;
 }
 
+int kaio_qkv_project_int4_noalloc(const void* x, const uint32_t* wq, const uint32_t* wk,
+                                  const uint32_t* wv, const void* sq, const void* sk, const void* sv,
+                                  void* q, void* k, void* v, uint32_t M, uint32_t N, uint32_t K,
+                                  kaio_stream_t stream_) {
+  g_last_error.clear();
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  const size_t m = M, n = N, kk = K;
+  const Span in[7] = {{"x", x, m * kk * 2},          {"w_q_packed", wq, kk / 8 * n * 4},
+                      {"w_k_packed", wk, kk / 8 * n * 4}, {"w_v_packed", wv, kk / 8 * n * 4},
+                      {"scales_q", sq, kk / 128 * n * 2}, {"scales_k", sk, kk / 128 * n * 2},
+                      {"scales_v", sv, kk / 128 * n * 2}};
+  const Span out[3] = {{"q", q, m * n * 2}, {"k", k, m * n * 2}, {"v", v, m * n * 2}};
+  KAIO_TRY(check_not_null(in, 7));
+  KAIO_TRY(check_not_null(out, 3));
+  if (M > 16)
+    return fail(KAIO_ERR_INVALID_VALUE,
+                "M (%u) exceeds 16: the allocation-free entry runs the decode kernel only", M);
+  if (K % 128 != 0)
+    return fail(KAIO_ERR_INVALID_VALUE, "K (%u) must be a multiple of group_size (128)", K);
+  if (N % 8 != 0)
+    return fail(KAIO_ERR_INVALID_VALUE, "N (%u) must be a multiple of 8 (16-byte rows)", N);
+  const uint64_t groups = 3ull * ((static_cast<uint64_t>(N) + 255) / 256);
+  if (groups > static_cast<uint64_t>(kaio::noalloc_max_counters()))
+    return fail(KAIO_ERR_INVALID_VALUE,
+                "N (%u) exceeds the allocation-free limit (%d column groups of 256 in its "
+                "fixed %zu-byte scratch)", N, kaio::noalloc_max_counters(), kaio::kNoAllocScratchBytes);
+  KAIO_TRY(check_aligned(in, 7));
+  KAIO_TRY(check_aligned(out, 3));
+  if (static_cast<uint64_t>(K) / 8 * N > 0x7FFFFFFFull)
+    return fail(KAIO_ERR_INVALID_VALUE, "problem too large (M=%u N=%u K=%u)", M, N, K);
+  KAIO_TRY(check_overlap(in, 7, out, 3));
+  int dev;
+  DeviceInfo info;
+  KAIO_TRY(current_device(&dev, &info));
+  if (M == 0 || N == 0) return KAIO_OK;
+  KAIO_TRY(check_on_device(out, 3, dev));
+  if (K == 0) return zero_outputs(out, 3, stream);
+  KAIO_TRY(check_on_device(in, 7, dev));
+  kaio::DecodeParams prm{};
+  prm.x = static_cast<const __half*>(x);
+  const uint32_t* w3[3] = {wq, wk, wv};
+  const void* s3[3] = {sq, sk, sv};
+  void* o3[3] = {q, k, v};
+  for (int i = 0; i < 3; ++i) {
+    prm.w[i] = w3[i];
+    prm.s[i] = static_cast<const __half*>(s3[i]);
+    prm.out[i] = static_cast<__half*>(o3[i]);
+  }
+  prm.M = static_cast<int>(M);
+  prm.N = static_cast<int>(N);
+  prm.K = static_cast<int>(K);
+  const cudaError_t e = kaio::launch_decode_noalloc(prm, dev, info.sms, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "allocation-free decode launch");
+  return KAIO_OK;
+}
+
 int kaio_matmul_tc(const void* a, const void* b, float* c, uint32_t M, uint32_t N, uint32_t K,
                    kaio_stream_t stream_) {
   g_last_error.clear();

@@ -31,6 +31,8 @@
 //   counter for the next launch.
 #include <cuda_fp16.h>
 
+#include <mutex>
+
 #include "kaio_device.cuh"
 #include "kaio_internal.h"
 
@@ -324,6 +326,88 @@ cudaError_t launch_decode(const DecodeParams& prm, const DecodePlan& pl, cudaStr
     if (e != cudaSuccess) return e;
     decode_w4a16_kernel<2><<<pl.ctas, kThreads, pl.smem, stream>>>(prm);
   }
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant of the decode launch.
+//
+// Some callers cannot allocate device memory: code that runs inside another
+// runtime's memory budget (inference engines and plugin hosts that hand out
+// every byte themselves and forbid cudaMalloc), processes whose device memory
+// is fully reserved up front, and real-time paths where an allocation's
+// implicit synchronisation or failure is not acceptable. For them the split-K
+// scratch of the decode kernel (per-group arrival counters and the partial
+// sums) lives in this fixed array instead of the workspace that
+// kaio_qkv_project_int4 allocates. Every GPU that loads the library holds
+// these bytes until the process exits. All calls share the one array: calls
+// whose kernels overlap on the GPU (different streams, no ordering between
+// them) race on it and give wrong results; order them on one stream.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+constexpr size_t kNoAllocCounterBytes = 64u << 10;                  // 16384 group counters
+static_assert(kNoAllocScratchBytes > kNoAllocCounterBytes, "scratch layout");
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+unsigned char* g_noalloc_ptr[kMaxDevices] = {};
+}  // namespace
+
+// Device address of the scratch array on the current device. The array's name
+// in host code is only a host-side stand-in, so the address is looked up once
+// per device (this first call should come before any stream capture).
+static cudaError_t noalloc_scratch(int dev, unsigned char** out) {
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    g_noalloc_ptr[dev] = static_cast<unsigned char*>(p);
+  }
+  *out = g_noalloc_ptr[dev];
+  return cudaSuccess;
+}
+
+int noalloc_max_counters() { return static_cast<int>(kNoAllocCounterBytes / sizeof(unsigned)); }
+
+cudaError_t launch_decode_noalloc(DecodeParams prm, int dev, int num_sms, cudaStream_t stream) {
+  unsigned char* base = nullptr;
+  cudaError_t e = noalloc_scratch(dev, &base);
+  if (e != cudaSuccess) return e;
+  // As many CTAs as the partial-sum region holds (all SMs on a GB300).
+  const int mt = (prm.M <= 8) ? 1 : 2;
+  const size_t per_cta = static_cast<size_t>(2) * kCW * 32 * 8 * mt * sizeof(float);
+  const int fit = static_cast<int>((kNoAllocScratchBytes - kNoAllocCounterBytes) / per_cta);
+  const DecodePlan pl = plan_decode(prm.M, prm.N, prm.K, std::min(num_sms, fit));
+  if (static_cast<size_t>(pl.counters) * sizeof(unsigned) > kNoAllocCounterBytes)
+    return cudaErrorInvalidValue;
+  prm.groups_per_proj = pl.groups_per_proj;
+  prm.nkb = pl.nkb;
+  prm.units = pl.units;
+  prm.ctas = pl.ctas;
+  prm.xmax_kb = pl.xmax_kb;
+  prm.counters = reinterpret_cast<unsigned*>(base);
+  prm.partials = reinterpret_cast<float*>(base + kNoAllocCounterBytes);
+  // The counters must start at zero; the array keeps whatever the last call left.
+  e = cudaMemsetAsync(prm.counters, 0, static_cast<size_t>(pl.counters) * sizeof(unsigned), stream);
+  if (e != cudaSuccess) return e;
+  const void* kern = (pl.mt == 1) ? reinterpret_cast<const void*>(decode_w4a16_kernel<1>)
+                                   : reinterpret_cast<const void*>(decode_w4a16_kernel<2>);
+  // Raise (never lower) the kernel's dynamic shared-memory limit.
+  cudaFuncAttributes fa{};
+  e = cudaFuncGetAttributes(&fa, kern);
+  if (e != cudaSuccess) return e;
+  if (static_cast<size_t>(fa.maxDynamicSharedSizeBytes) < pl.smem) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(pl.smem));
+    if (e != cudaSuccess) return e;
+  }
+  if (pl.mt == 1)
+    decode_w4a16_kernel<1><<<pl.ctas, kThreads, pl.smem, stream>>>(prm);
+  else
+    decode_w4a16_kernel<2><<<pl.ctas, kThreads, pl.smem, stream>>>(prm);
   return cudaGetLastError();
 }
 

@@ -43,6 +43,13 @@ struct DecodePlan {
 DecodePlan plan_decode(int M, int N, int K, int num_sms);
 cudaError_t launch_decode(const DecodeParams& prm, const DecodePlan& pl, cudaStream_t stream);
 
+// Allocation-free decode launch: split-K scratch in a fixed device array of
+// kNoAllocScratchBytes (the first 64 KiB hold group counters). `prm` needs only
+// the tensors and M, N, K; the plan and scratch pointers are filled in here.
+constexpr size_t kNoAllocScratchBytes = 8u << 20;
+int noalloc_max_counters();
+cudaError_t launch_decode_noalloc(DecodeParams prm, int dev, int num_sms, cudaStream_t stream);
+
 // ------------------------------------------------- tensor-core (tcgen05) paths
 struct GemmShape {
   int M, N, K;              // C[M, N] = sum_k Aop[M, k] * Bop[k, N]

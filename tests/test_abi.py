@@ -134,3 +134,15 @@ def test_binding_refuses_cpu_tensors():
         kaio.qkv_project_int4(x, w, w, w, s, s, s)
     with pytest.raises(ValueError, match="CUDA device"):
         kaio.matmul_tc(torch.zeros(8, 8, dtype=torch.float16), torch.zeros(8, 8, dtype=torch.float16))
+
+
+def test_noalloc_entry_validation(L):
+    p = [ptr(j) for j in range(10)]
+    assert L.kaio_qkv_project_int4_noalloc(*p, 17, 128, 256, None) == INVALID     # M > 16
+    assert "exceeds 16" in kaio.last_error()
+    assert L.kaio_qkv_project_int4_noalloc(*p, 16, 128, 200, None) == INVALID     # K % 128
+    assert L.kaio_qkv_project_int4_noalloc(*p, 16, 5462 * 256, 128, None) == INVALID
+    assert "allocation-free limit" in kaio.last_error()
+    q = list(p)
+    q[4] += 2
+    assert L.kaio_qkv_project_int4_noalloc(*q, 16, 128, 256, None) == MISALIGNED
