@@ -14,6 +14,8 @@
 
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
+#include <cstring>
 #include <map>
 #include <mutex>
 #include <string>
@@ -244,6 +246,31 @@ int kaio_qkv_project_int4(const void* x, const uint32_t* wq, const uint32_t* wk,
   if (kaio_qkv_path(M) == 0) {
     const kaio::DecodePlan pl = kaio::plan_decode(static_cast<int>(M), static_cast<int>(N),
                                                   static_cast<int>(K), info.sms);
+    // Default: the tcgen05 decode kernel (cluster split-K). KAIO_DECODE_SPLIT
+    // selects one of the three decode kernels instead -- "tc", "mma" (mma.sync,
+    // cluster split-K) or "streamk" (mma.sync, stream-K split with a workspace);
+    // all three compute the same result.
+    const char* force = std::getenv("KAIO_DECODE_SPLIT");
+    const bool want_mma = force && std::strcmp(force, "mma") == 0;
+    const bool want_streamk = force && std::strcmp(force, "streamk") == 0;
+    if (!want_mma && !want_streamk) {
+      const kaio::TcDecodePlan tp = kaio::plan_tc_decode(static_cast<int>(M), static_cast<int>(N),
+                                                         static_cast<int>(K), dev);
+      if (tp.ok) {
+        e = kaio::launch_tc_decode(static_cast<const __half*>(x), w3, s3, o3, static_cast<int>(M),
+                                   static_cast<int>(N), static_cast<int>(K), tp, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "tcgen05 decode kernel launch");
+        return KAIO_OK;
+      }
+    }
+    const kaio::ClusterPlan cp = kaio::plan_decode_cluster(static_cast<int>(M), static_cast<int>(N),
+                                                           static_cast<int>(K), info.sms, dev);
+    if (cp.ok && !want_streamk) {
+      e = kaio::launch_decode_cluster(static_cast<const __half*>(x), w3, s3, o3, static_cast<int>(M),
+                                      static_cast<int>(N), static_cast<int>(K), cp, stream);
+      if (e != cudaSuccess) return cuda_fail(e, "cluster decode kernel launch");
+      return KAIO_OK;
+    }
     unsigned* counters = nullptr;
     float* partials = nullptr;
     KAIO_TRY(get_workspace(dev, stream, pl.counters, pl.partial_floats, &counters, &partials));
@@ -432,8 +459,12 @@ int kaio_device_status(void) {
   g_last_error.clear();
   cudaError_t e = cudaDeviceSynchronize();
   if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
-  const unsigned err = kaio::read_and_clear_tc_errors();
-  if (err == 0xFFFFFFFFu) return fail(KAIO_ERR_CUDA, "could not read the device error word");
+  const unsigned err_tc = kaio::read_and_clear_tc_errors();
+  const unsigned err_dc = kaio::read_and_clear_decode_errors();
+  const unsigned err_td = kaio::read_and_clear_tc_decode_errors();
+  if (err_tc == 0xFFFFFFFFu || err_dc == 0xFFFFFFFFu || err_td == 0xFFFFFFFFu)
+    return fail(KAIO_ERR_CUDA, "could not read the device error word");
+  const unsigned err = err_tc | err_dc | err_td;
   if (err & kaio::kDevErrTimeoutHost)
     return fail(KAIO_ERR_DEVICE_TIMEOUT, "a kernel gave up a bounded wait (device error word 0x%x)", err);
   return KAIO_OK;

@@ -33,6 +33,7 @@
 
 #include <mutex>
 
+#include "decode_frag.cuh"
 #include "kaio_device.cuh"
 #include "kaio_internal.h"
 
@@ -45,69 +46,6 @@ constexpr int kWarps = kCW * kKW;      // 16
 constexpr int kThreads = kWarps * 32;  // 512
 constexpr int kGroupCols = kCW * 32;   // 256 output columns per group
 constexpr int kDepth = 4;              // k-blocks of weights in flight per warp
-
-template <int MT>
-struct Frag {
-  static constexpr int kRows = 8 * MT;        // padded batch rows
-  static constexpr int kAcc = 8 * MT;         // f32 accumulators per thread
-  static constexpr int kXkb = 128 * kRows;    // bytes of staged x per k-block
-};
-
-struct Ring {
-  uint4 w0, w1;  // packed rows 2t and 2t+1, columns 4g .. 4g+3
-  uint2 sc;      // scales of those 4 columns
-};
-
-__device__ __forceinline__ void load_ring(Ring& r, const uint32_t* __restrict__ w,
-                                          const __half* __restrict__ s, int N, int kb, int col,
-                                          int t, bool valid) {
-  if (valid) {
-    const uint32_t* p = w + static_cast<size_t>(kb * 8 + 2 * t) * N + col;
-    r.w0 = ldg_stream_v4(p);
-    r.w1 = ldg_stream_v4(p + N);
-    r.sc = __ldg(reinterpret_cast<const uint2*>(s + static_cast<size_t>(kb >> 1) * N + col));
-  } else {
-    r.w0 = make_uint4(0, 0, 0, 0);
-    r.w1 = r.w0;
-    r.sc = make_uint2(0, 0);
-  }
-}
-
-template <int MT>
-__device__ __forceinline__ void compute_kb(float (&acc)[2][MT][4], const Ring& r,
-                                           const unsigned char* xs_kb, int g, int t) {
-  constexpr int R = Frag<MT>::kRows;
-  uint4 xa[MT], xb[MT];
-#pragma unroll
-  for (int nt = 0; nt < MT; ++nt) {
-    const unsigned char* base = xs_kb + (g + 8 * nt) * 64 + t * 16;
-    xa[nt] = *reinterpret_cast<const uint4*>(base);
-    xb[nt] = *reinterpret_cast<const uint4*>(base + 64 * R);
-  }
-  const uint32_t s2[4] = {
-      __byte_perm(r.sc.x, 0, 0x1010), __byte_perm(r.sc.x, 0, 0x3232),
-      __byte_perm(r.sc.y, 0, 0x1010), __byte_perm(r.sc.y, 0, 0x3232)};
-  const PairedNibbles q0[4] = {PairedNibbles(r.w0.x), PairedNibbles(r.w0.y),
-                               PairedNibbles(r.w0.z), PairedNibbles(r.w0.w)};
-  const PairedNibbles q1[4] = {PairedNibbles(r.w1.x), PairedNibbles(r.w1.y),
-                               PairedNibbles(r.w1.z), PairedNibbles(r.w1.w)};
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    uint32_t b0[MT], b1[MT];
-#pragma unroll
-    for (int nt = 0; nt < MT; ++nt) {
-      b0[nt] = (j == 0) ? xa[nt].x : (j == 1) ? xa[nt].y : (j == 2) ? xa[nt].z : xa[nt].w;
-      b1[nt] = (j == 0) ? xb[nt].x : (j == 1) ? xb[nt].y : (j == 2) ? xb[nt].z : xb[nt].w;
-    }
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const uint32_t a[4] = {q0[2 * i].pair(j, s2[2 * i]), q0[2 * i + 1].pair(j, s2[2 * i + 1]),
-                             q1[2 * i].pair(j, s2[2 * i]), q1[2 * i + 1].pair(j, s2[2 * i + 1])};
-#pragma unroll
-      for (int nt = 0; nt < MT; ++nt) mma_16816(acc[i][nt], a, b0[nt], b1[nt]);
-    }
-  }
-}
 
 // Unit range of CTA c: [c*U/G, (c+1)*U/G).
 __device__ __forceinline__ long long unit_begin(long long c, long long U, long long G) {

@@ -50,6 +50,40 @@ constexpr size_t kNoAllocScratchBytes = 8u << 20;
 int noalloc_max_counters();
 cudaError_t launch_decode_noalloc(DecodeParams prm, int dev, int num_sms, cudaStream_t stream);
 
+// Cluster split-K decode (no scratch): a column group of 256 outputs per cluster
+// of S CTAs, each CTA one contiguous range of 128-row K groups.
+struct ClusterPlan {
+  bool ok;
+  int mt;
+  int groups_per_proj, groups;  // column groups over the three projections
+  int ng;                       // K / 128
+  int S;                        // cluster size
+  int nst;                      // ring stages (16 KB each)
+  int sbox;                     // scale rows per TMA box
+  int s_off, x_off;             // shared-memory layout
+  size_t smem;
+  long long est_groups;         // K groups streamed by the busiest SM (cost estimate)
+};
+ClusterPlan plan_decode_cluster(int M, int N, int K, int num_sms, int dev);
+cudaError_t launch_decode_cluster(const __half* x, const uint32_t* const w[3],
+                                  const __half* const s[3], __half* const out[3], int M, int N, int K,
+                                  const ClusterPlan& pl, cudaStream_t stream);
+unsigned read_and_clear_decode_errors();
+
+// tcgen05 decode (M <= 16): 128-column tiles over the three projections, split
+// over K across a cluster of S CTAs.
+struct TcDecodePlan {
+  bool ok;
+  int tiles;   // ceil(N / 128)
+  int ng;      // K / 128
+  int S;       // cluster size
+};
+TcDecodePlan plan_tc_decode(int M, int N, int K, int dev);
+cudaError_t launch_tc_decode(const __half* x, const uint32_t* const w[3], const __half* const s[3],
+                             __half* const out[3], int M, int N, int K, const TcDecodePlan& pl,
+                             cudaStream_t stream);
+unsigned read_and_clear_tc_decode_errors();
+
 // ------------------------------------------------- tensor-core (tcgen05) paths
 struct GemmShape {
   int M, N, K;              // C[M, N] = sum_k Aop[M, k] * Bop[k, N]

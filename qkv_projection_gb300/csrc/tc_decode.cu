@@ -1,0 +1,487 @@
+// W4A16 fused QKV projection for decode-sized M (1..16) on the 5th-generation
+// tensor cores, split over K across the CTAs of a thread-block cluster.
+//
+// What it computes ("kaio-candle -- src/qkv_project_int4.rs", doc comment of
+// qkv_project_int4): out_p[m, n] = f16(sum_k x[m, k] * RN_f16(int4(W_p[k, n]) *
+// s_p[k/128, n])), f32 accumulation, f32 -> f16 in-kernel.
+//
+// The legacy mma.sync path runs at about a tenth of the tcgen05 rate on this
+// GPU, which is below what M = 16 needs to keep up with HBM. Here the product is
+// taken transposed, D_p[n, m] = Wd_p^T x^T, on tcgen05 with M = 128 output
+// columns (TMEM lanes), N = 16 padded batch rows and K = 16 per instruction:
+// * a producer warp streams, per K group of 128 rows, the 16 x 128 packed words
+//   and the scale row of each projection plus two 64-wide 128B-swizzled x boxes
+//   (rows >= M are zero-filled by TMA) into a ring of shared-memory stages;
+// * sixteen dequant warps (thread = output column = TMEM lane) turn packed
+//   words into f16 operands in registers and store them into TMEM A stages;
+// * two MMA warps issue tcgen05.mma (A from TMEM, B = x tile from shared
+//   memory) into their own f32 accumulators: at N = 16 the per-instruction
+//   issue cost of one warp would leave the tensor core idle most of the time,
+//   and two issuers overlap it;
+// * the CTAs of a cluster cover consecutive K ranges of the same 128 columns;
+//   their accumulators are reduced through distributed shared memory, in rank
+//   order (deterministic), and written as f16.
+// The kernel takes all 512 TMEM columns; its shared memory keeps it alone on an
+// SM, so no CTA ever waits for TMEM. Every
+// mbarrier wait is bounded, and both cluster barriers are reached by every
+// thread whatever happens.
+#include <cuda.h>
+#include <cuda_fp16.h>
+
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "kaio_device.cuh"
+#include "kaio_internal.h"
+
+namespace kaio {
+
+__device__ unsigned g_td_err = 0;
+
+namespace {
+
+constexpr int DN = 128;                  // output columns per CTA (TMEM lanes, MMA M)
+constexpr int DM = 16;                   // padded batch rows (MMA N)
+constexpr int DGPS = 2;                          // K groups (of 128 K) per shared-memory stage
+constexpr int DXBOX = DM * 64 * 2;               // one 64-K x box, 16 rows, 128B-swizzled: 2 KB
+constexpr int DX_STAGE = DGPS * 2 * DXBOX;       // 8 KB
+constexpr int DW_BOX = DGPS * 16 * DN * 4;       // 32 packed rows x 128 columns: 16 KB
+constexpr int DSTAGE_BYTES = DX_STAGE + 3 * DW_BOX;   // 56 KB, multiple of 1024
+constexpr int DMAX_STAGES = 4;
+constexpr int DSCALE_ROW = 3 * DN * 2;           // the three scale rows of one K group: 768 B
+constexpr int DDQ_WARPS = 16;                    // 4 per TMEM lane quadrant
+constexpr int DMMA_WARPS = 2;                    // each issues half of the 16-K MMA steps
+constexpr int DTHREADS = (1 + DMMA_WARPS + DDQ_WARPS) * 32;   // 608
+constexpr int DASTAGES = 2;                      // TMEM A stages of one K group (128 K)
+constexpr uint32_t DTMEM_COLS = 512;
+constexpr uint32_t DA_COL0 = 128;                // accumulators D[q][w] at 0..95, A stages after
+constexpr uint32_t DA_STAGE_COLS = 192;          // 3 projections x 64 columns (128 K)
+constexpr int DRED_BYTES = 3 * DM * DN * 4;      // one CTA's partial tile (24 KB)
+constexpr int DSMEM_LIMIT = 232448 - 1024;       // opt-in per-block limit minus static shared memory
+constexpr size_t DSMEM = DSMEM_LIMIT;
+static_assert(DSTAGE_BYTES % 1024 == 0, "x boxes stay 1024-aligned");
+static_assert(DRED_BYTES <= DSTAGE_BYTES, "partials reuse the ring");
+static_assert(DA_COL0 + DASTAGES * DA_STAGE_COLS <= DTMEM_COLS, "TMEM layout");
+
+struct DecTcParams {
+  __half* out[3];
+  int M, N, K;
+  int tiles;     // ceil(N / 128) column tiles (each covers Q, K and V)
+  int S;         // cluster size: K ranges per column tile
+  int ng;        // K / 128
+  int nst;       // ring stages (DGPS K groups each)
+  int s_off;     // byte offset of the scale rows (after the ring)
+  int sbox;      // scale rows per TMA box
+};
+
+// K order inside every 16-byte chunk of a staged x box is changed from
+// (0..7) to (0,4,1,5,2,6,3,7): the dequantised weights come out of the mask
+// trick as nibble pairs (j, j+4), and A and B must agree on the K order.
+__device__ __forceinline__ void permute_x_chunk(unsigned char* p) {
+  uint4 v = *reinterpret_cast<const uint4*>(p);
+  uint4 o;
+  o.x = __byte_perm(v.x, v.z, 0x5410);
+  o.y = __byte_perm(v.x, v.z, 0x7632);
+  o.z = __byte_perm(v.y, v.w, 0x5410);
+  o.w = __byte_perm(v.y, v.w, 0x7632);
+  *reinterpret_cast<uint4*>(p) = o;
+}
+
+// tcgen05.mma kind::f16, A from TMEM, B descriptor given as two 32-bit halves.
+__device__ __forceinline__ void umma_ts_lohi(uint32_t d, uint32_t a, uint32_t lo, uint32_t hi,
+                                             uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 bd;\n\tsetp.ne.b32 p, %5, 0;\n\tmov.b64 bd, {%2, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], bd, %4, p;\n\t}" ::"r"(d),
+      "r"(a), "r"(lo), "r"(hi), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__global__ void __launch_bounds__(DTHREADS, 1)
+    tc_decode_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW0,
+                     const __grid_constant__ CUtensorMap tmW1, const __grid_constant__ CUtensorMap tmW2,
+                     const __grid_constant__ CUtensorMap tmS0, const __grid_constant__ CUtensorMap tmS1,
+                     const __grid_constant__ CUtensorMap tmS2, const DecTcParams p) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  __shared__ __align__(8) uint64_t full[DMAX_STAGES], empty[DMAX_STAGES], sbar, a_full[DASTAGES],
+      a_empty[DASTAGES], acc_full, mma_done[DMMA_WARPS];
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_flag;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rank = static_cast<int>(cluster_ctarank());
+  const int tile = blockIdx.x / p.S;
+  const int n0 = tile * DN;
+  const int g_begin = rank * p.ng / p.S;
+  const int nsg = (rank + 1) * p.ng / p.S - g_begin;     // K groups of this CTA
+  const int nstg = (nsg + DGPS - 1) / DGPS;              // shared-memory stages of this CTA
+  volatile int* abort = &abort_flag;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < p.nst; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], DDQ_WARPS + DMMA_WARPS);   // dequant warps + one commit per MMA warp
+    }
+    mbar_init(&sbar, 1);
+    for (int a = 0; a < DASTAGES; ++a) {
+      mbar_init(&a_full[a], DDQ_WARPS);
+      mbar_init(&a_empty[a], DMMA_WARPS);
+    }
+    mbar_init(&acc_full, DMMA_WARPS);
+    for (int w = 0; w < DMMA_WARPS; ++w) mbar_init(&mma_done[w], 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(&tmem_base_sh, DTMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    // Few, large copies: per stage one 16 KB box of packed words per projection
+    // and four 2 KB x boxes; the scale rows of the whole K range up front.
+    if (lane == 0) {
+      tma_prefetch_desc(&tmX);
+      tma_prefetch_desc(&tmW0); tma_prefetch_desc(&tmW1); tma_prefetch_desc(&tmW2);
+      tma_prefetch_desc(&tmS0); tma_prefetch_desc(&tmS1); tma_prefetch_desc(&tmS2);
+      const int nsb = (nsg + p.sbox - 1) / p.sbox;
+      mbar_arrive_expect_tx(&sbar, static_cast<uint32_t>(3 * nsb * p.sbox * DN * 2));
+      for (int b = 0; b < nsb; ++b) {
+        unsigned char* ss = smem + p.s_off + b * p.sbox * DSCALE_ROW;
+        tma_load_2d(ss, &tmS0, &sbar, n0, g_begin + b * p.sbox);
+        tma_load_2d(ss + p.sbox * DN * 2, &tmS1, &sbar, n0, g_begin + b * p.sbox);
+        tma_load_2d(ss + 2 * p.sbox * DN * 2, &tmS2, &sbar, n0, g_begin + b * p.sbox);
+      }
+      uint32_t fills[DMAX_STAGES] = {0, 0, 0, 0};
+      int st = 0;
+      uint32_t ph = 0;
+      for (int i = 0; i < nstg; ++i) {
+        if (i >= p.nst && !mbar_wait(&empty[st], ph ^ 1, abort, &g_td_err)) break;
+        ++fills[st];
+        unsigned char* sx = smem + st * DSTAGE_BYTES;
+        unsigned char* sw = sx + DX_STAGE;
+        const int g = g_begin + i * DGPS;
+        mbar_arrive_expect_tx(&full[st], DSTAGE_BYTES);
+        tma_load_2d(sw, &tmW0, &full[st], n0, g * 16);
+        tma_load_2d(sw + DW_BOX, &tmW1, &full[st], n0, g * 16);
+        tma_load_2d(sw + 2 * DW_BOX, &tmW2, &full[st], n0, g * 16);
+#pragma unroll
+        for (int b = 0; b < 2 * DGPS; ++b)
+          tma_load_2d(sx + b * DXBOX, &tmX, &full[st], (g * 2 + b) * 64, 0);
+        if (++st == p.nst) { st = 0; ph ^= 1; }
+      }
+      for (int s2 = 0; s2 < p.nst; ++s2)
+        if (fills[s2]) mbar_wait_drain(&full[s2], (fills[s2] - 1) & 1, &g_td_err);
+      mbar_wait_drain(&sbar, 0, &g_td_err);
+    }
+  } else if (warp <= DMMA_WARPS) {
+    // ------------------------------------------------------------ MMA warps
+    // MMA warp w owns the 16-K steps 2w and 2w+1 of each 64-K half of every K
+    // group: when a stage lands it permutes the x chunks of those steps, then
+    // per K group issues their MMAs into its own accumulators D[q][w]. Two
+    // issuing warps overlap the per-instruction issue cost, which dominates at
+    // N = 16.
+    const int w = warp - 1;
+    constexpr uint32_t idesc = idesc_f16_f32(DN, DM, false, false);
+    int a = 0, st = 0;
+    uint32_t aph = 0, ph = 0;
+    bool ok = true;
+    for (int i = 0; i < nstg && ok; ++i) {
+      if (!mbar_wait(&full[st], ph, abort, &g_td_err)) { ok = false; break; }
+      unsigned char* sx = smem + st * DSTAGE_BYTES;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {                // 256 chunks: 4 boxes x 16 rows x 4 chunks
+        const int t = lane * 8 + u;
+        const int b = t >> 6, m = (t >> 2) & 15, c = 4 * w + (t & 3);
+        permute_x_chunk(sx + b * DXBOX + (m >> 3) * 1024 + (m & 7) * 128 + ((c ^ (m & 7)) << 4));
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      const uint64_t bd0 = sdesc_sw128(smem_u32(sx), 16, 1024);
+      const uint32_t blo = static_cast<uint32_t>(bd0), bhi = static_cast<uint32_t>(bd0 >> 32);
+      const int ngs = min(DGPS, nsg - i * DGPS);
+      for (int j = 0; j < ngs; ++j) {              // K groups of this stage
+        if (!mbar_wait(&a_full[a], aph, abort, &g_td_err)) { ok = false; break; }
+        if (lane == 0) {
+          tc_fence_after();
+          const uint32_t acc0 = (i | j) != 0 ? 1u : 0u;
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+            for (int k2 = 0; k2 < 2; ++k2) {
+              const int kk = 2 * w + k2;
+              const uint32_t lo = blo + static_cast<uint32_t>(((2 * j + hh) * DXBOX + kk * 32) >> 4);
+#pragma unroll
+              for (int q = 0; q < 3; ++q)
+                umma_ts_lohi(tmem + (q * 2 + w) * DM,
+                             tmem + DA_COL0 + a * DA_STAGE_COLS + q * 64 + kk * 16 + hh * 8, lo, bhi,
+                             idesc, (hh | k2) != 0 ? 1u : acc0);
+            }
+          umma_commit(&a_empty[a]);
+          if (j == ngs - 1) umma_commit(&empty[st]);
+        }
+        __syncwarp();
+        if (++a == DASTAGES) { a = 0; aph ^= 1; }
+      }
+      if (++st == p.nst) { st = 0; ph ^= 1; }
+    }
+    if (lane == 0) {
+      if (ok) umma_commit(&acc_full);              // fires when this warp's MMAs are done
+      umma_commit(&mma_done[w]);
+      mbar_wait_drain(&mma_done[w], 0, &g_td_err);
+    }
+  } else {
+    // ------------------------------------------------------------ dequant warps
+    // Thread = output column n0 + 32*sp + lane = TMEM lane. Quarter qr fills
+    // the 16-K MMA step qr of both 64-K halves of each K group (packed rows
+    // 2qr, 2qr+1 and 8+2qr, 9+2qr): 16 TMEM columns per projection, one store.
+    const int sp = warp & 3;
+    const int qr = (warp - 1 - DMMA_WARPS) >> 2;
+    const int nl = 32 * sp + lane;
+    const uint32_t lane_base = static_cast<uint32_t>(32 * sp) << 16;
+    const unsigned char* scale_base = smem + p.s_off + nl * 2;
+    int a = 0, st = 0;
+    uint32_t aph = 0, ph = 0;
+    bool ok = mbar_wait(&sbar, 0, abort, &g_td_err);
+    int gl = 0;                                     // group index inside the CTA's range
+    for (int i = 0; i < nstg && ok; ++i) {
+      if (!mbar_wait(&full[st], ph, abort, &g_td_err)) { ok = false; break; }
+      const unsigned char* sw = smem + st * DSTAGE_BYTES + DX_STAGE + (2 * qr) * (DN * 4) + nl * 4;
+      const int ngs = min(DGPS, nsg - i * DGPS);
+      for (int j = 0; j < ngs && ok; ++j, ++gl) {
+        // scale rows of group gl: box gl/8 (boxes hold up to 8 rows), row gl%8
+        const unsigned char* sc = scale_base + (gl >> 3) * p.sbox * DSCALE_ROW + (gl & 7) * (DN * 2);
+        uint32_t wd[3][4], s2[3];
+#pragma unroll
+        for (int q = 0; q < 3; ++q) {
+          const uint16_t sb = *reinterpret_cast<const uint16_t*>(sc + q * p.sbox * DN * 2);
+          s2[q] = half2_bits(sb, sb);
+          const unsigned char* wq = sw + q * DW_BOX + j * 16 * (DN * 4);
+          wd[q][0] = *reinterpret_cast<const uint32_t*>(wq);
+          wd[q][1] = *reinterpret_cast<const uint32_t*>(wq + DN * 4);
+          wd[q][2] = *reinterpret_cast<const uint32_t*>(wq + 8 * DN * 4);
+          wd[q][3] = *reinterpret_cast<const uint32_t*>(wq + 9 * DN * 4);
+        }
+        if (j == ngs - 1) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&empty[st]);   // packed words of this stage are in registers
+        }
+        if (!mbar_wait(&a_empty[a], aph ^ 1, abort, &g_td_err)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t tbase = tmem + lane_base + DA_COL0 + a * DA_STAGE_COLS + qr * 16;
+#pragma unroll
+        for (int q = 0; q < 3; ++q) {
+          uint32_t v[16];
+#pragma unroll
+          for (int r = 0; r < 4; ++r) {
+            const PairedNibbles pn(wd[q][r]);
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) v[4 * r + jj] = pn.pair(jj, s2[q]);
+          }
+          tmem_st16(tbase + q * 64, v);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&a_full[a]);
+        if (++a == DASTAGES) { a = 0; aph ^= 1; }
+      }
+      if (++st == p.nst) { st = 0; ph ^= 1; }
+    }
+
+    // Epilogue part 1: this CTA's partial sum_w D[q][w][n][m] -> shared
+    // red[q][m][n] (quarter qr drains batch rows 4qr .. 4qr+3). The ring is free
+    // once every MMA has completed (acc_full).
+    float* red = reinterpret_cast<float*>(smem);
+    const bool have = ok && nsg > 0 && mbar_wait(&acc_full, 0, abort, &g_td_err);
+    if (have) tc_fence_after();
+#pragma unroll
+    for (int q = 0; q < 3; ++q) {
+      float sum[4] = {0.f, 0.f, 0.f, 0.f};
+      if (have) {
+#pragma unroll
+        for (int w2 = 0; w2 < DMMA_WARPS; ++w2) {
+          uint32_t r[4];
+          tmem_ld4(tmem + lane_base + (q * 2 + w2) * DM + qr * 4, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) sum[jj] += __uint_as_float(r[jj]);
+        }
+      }
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) red[(q * DM + qr * 4 + jj) * DN + nl] = sum[jj];
+    }
+    tc_fence_before();
+  }
+
+  // Epilogue part 2: rank r finishes batch rows m with m % S == r, summing the
+  // S partials in rank order through distributed shared memory, four columns
+  // at a time.
+  __syncwarp();
+  cluster_sync_all();
+  {
+    const int dt = threadIdx.x;
+    const uint32_t red_s = smem_u32(smem);
+    const int rows = (p.M - rank + p.S - 1) / p.S;      // rows rank, rank+S, ... below M
+    const int items = rows * 3 * (DN / 4);
+    for (int it = dt; it < items; it += DTHREADS) {
+      const int m = rank + (it / (3 * (DN / 4))) * p.S;
+      const int q = (it / (DN / 4)) % 3;
+      const int n4 = it % (DN / 4);
+      const uint32_t off = static_cast<uint32_t>(((q * DM + m) * DN + 4 * n4) * 4);
+      float4 v[8];
+#pragma unroll
+      for (int r = 0; r < 8; ++r)
+        if (r < p.S) v[r] = dsmem_ld_f4(dsmem_map(red_s + off, static_cast<uint32_t>(r)));
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int r = 0; r < 8; ++r)
+        if (r < p.S) {
+          acc.x += v[r].x; acc.y += v[r].y; acc.z += v[r].z; acc.w += v[r].w;
+        }
+      const int c4 = n0 + 4 * n4;
+      if (c4 < p.N) {
+        __half* out = q == 0 ? p.out[0] : (q == 1 ? p.out[1] : p.out[2]);
+        const __half2 lo = __floats2half2_rn(acc.x, acc.y);
+        const __half2 hi = __floats2half2_rn(acc.z, acc.w);
+        uint2 u;
+        u.x = *reinterpret_cast<const uint32_t*>(&lo);
+        u.y = *reinterpret_cast<const uint32_t*>(&hi);
+        *reinterpret_cast<uint2*>(out + static_cast<size_t>(m) * p.N + c4) = u;
+      }
+    }
+  }
+  __syncwarp();
+  cluster_sync_all();
+  if (warp == 0) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, DTMEM_COLS);
+  }
+}
+
+int dec_max_active_clusters(int S, int dev) {
+  static std::mutex mu;
+  static std::map<std::pair<int, int>, int> cache;
+  std::lock_guard<std::mutex> lk(mu);
+  const auto key = std::make_pair(dev, S);
+  auto it = cache.find(key);
+  if (it != cache.end()) return it->second;
+  int n = 0;
+  const void* kern = reinterpret_cast<const void*>(tc_decode_kernel);
+  if (ensure_smem_limit(kern, static_cast<int>(DSMEM)) == cudaSuccess) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>(S * 64));
+    cfg.blockDim = dim3(DTHREADS);
+    cfg.dynamicSmemBytes = 120 * 1024;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(S);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+      cudaGetLastError();
+      n = 0;
+    }
+  }
+  cache[key] = n;
+  return n;
+}
+
+}  // namespace
+
+TcDecodePlan plan_tc_decode(int M, int N, int K, int dev) {
+  TcDecodePlan pl{};
+  pl.tiles = (N + DN - 1) / DN;
+  pl.ng = K / 128;
+  double best = -1;
+  for (int S = 1; S <= 8 && S <= pl.ng; ++S) {
+    const int range = (pl.ng + S - 1) / S;
+    const int sbytes = ((range + 7) / 8) * 8 * DSCALE_ROW;
+    if (sbytes + 2 * DSTAGE_BYTES + 2048 > DSMEM_LIMIT) continue;   // scales + 2 stages must fit
+    const int slots = dec_max_active_clusters(S, dev);
+    if (slots <= 0) continue;
+    const long long waves = (pl.tiles + slots - 1) / slots;
+    // Cost: K groups the busiest SM streams, plus a fixed start-up cost per wave.
+    const double est = static_cast<double>(waves) * (range + 2.0);
+    if (best < 0 || est < best - 1e-9) {
+      best = est;
+      pl.S = S;
+    }
+  }
+  pl.ok = best > 0 && M <= DM;
+  return pl;
+}
+
+cudaError_t launch_tc_decode(const __half* x, const uint32_t* const w[3], const __half* const s[3],
+                             __half* const out[3], int M, int N, int K, const TcDecodePlan& pl,
+                             cudaStream_t stream) {
+  const int range = (pl.ng + pl.S - 1) / pl.S;
+  const int sbox = std::min(8, pl.ng);
+  const int sbytes = ((range + sbox - 1) / sbox) * sbox * DSCALE_ROW;
+  DecTcParams p{};
+  for (int q = 0; q < 3; ++q) p.out[q] = out[q];
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.tiles = pl.tiles;
+  p.S = pl.S;
+  p.ng = pl.ng;
+  p.sbox = sbox;
+  const int nstg = (range + DGPS - 1) / DGPS;
+  p.nst = std::min(std::min(nstg, DMAX_STAGES), (DSMEM_LIMIT - 1024 - sbytes) / DSTAGE_BYTES);
+  p.nst = std::max(p.nst, 1);
+  p.s_off = p.nst * DSTAGE_BYTES;
+  const size_t smem_used = static_cast<size_t>(p.s_off + sbytes + 1024);
+  CUtensorMap tx, tw[3], ts[3];
+  CUresult r = encode_tensor_map_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, x, K, M,
+                                    static_cast<uint64_t>(K) * 2, 64, DM, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  for (int q = 0; q < 3; ++q) {
+    r = encode_tensor_map_2d(&tw[q], CU_TENSOR_MAP_DATA_TYPE_UINT32, w[q], N, K / 8,
+                             static_cast<uint64_t>(N) * 4, DN, DGPS * 16, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    r = encode_tensor_map_2d(&ts[q], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, s[q], N, K / 128,
+                             static_cast<uint64_t>(N) * 2, DN, sbox, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  }
+  cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(tc_decode_kernel), static_cast<int>(DSMEM));
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(pl.tiles * pl.S));
+  cfg.blockDim = dim3(DTHREADS);
+  // Always more than half the SM's shared memory: the kernel takes all of TMEM
+  // and must be alone on its SM.
+  cfg.dynamicSmemBytes = std::max(smem_used, static_cast<size_t>(120 * 1024));
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(pl.S);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, tc_decode_kernel, tx, tw[0], tw[1], tw[2], ts[0], ts[1], ts[2], p);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+unsigned read_and_clear_tc_decode_errors() {
+  unsigned v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_td_err, sizeof(v)) != cudaSuccess) return 0xFFFFFFFFu;
+  const unsigned zero = 0;
+  cudaMemcpyToSymbol(g_td_err, &zero, sizeof(zero));
+  return v;
+}
+
+}  // namespace kaio

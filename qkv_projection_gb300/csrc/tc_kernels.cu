@@ -202,6 +202,7 @@ __global__ void __launch_bounds__(GTHREADS, 1)
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
+    __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, GTMEM_COLS);
   }
@@ -430,6 +431,7 @@ __global__ void __launch_bounds__(PTHREADS, 1)
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
+    __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, PTMEM_COLS);
   }
