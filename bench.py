@@ -226,7 +226,11 @@ def run_kaio(args, cfg_name, ws, rank, local, dist):
         units_bytes = wbytes
         alg_bytes = wbytes + obytes
         flops = qkv_flops(M, N, K)
-        kernel_file = "decode_w4a16.cu" if kaio.qkv_path(M) == 0 else "tc_kernels.cu"
+        if kaio.qkv_path(M) == 0:
+            split = os.environ.get("KAIO_DECODE_SPLIT", "")
+            kernel_file = {"mma": "decode_cluster.cu", "streamk": "decode_w4a16.cu"}.get(split, "tc_decode.cu")
+        else:
+            kernel_file = "tc_kernels.cu"
         bound = "hbm" if M <= 16 else "tensor"
         launches_per_step = 1
     else:
@@ -415,13 +419,13 @@ def run_reference(args, cfg_name, ws, rank):
         return None
     if kind != "qkv":
         return {"impl": "reference", "unavailable": "oracle arm covers the W4A16 workloads only"}
-    # Size each step's sample so the whole run takes about a minute.
+    # Size each step's sample so the whole run takes about --ref-seconds.
     total_steps = args.steps + max(args.warmup, 3)
     probe, _, _ = oracle_step_fn(cfg_name, 1.0 / 64)
     t0 = time.perf_counter()
     probe()
     per_col = (time.perf_counter() - t0) / max(8, N // 64)
-    frac = min(1.0, max(8.0 / N, 60.0 / total_steps / max(per_col, 1e-9) / N))
+    frac = min(1.0, max(8.0 / N, args.ref_seconds / total_steps / max(per_col, 1e-9) / N))
     step, wb, ncols = oracle_step_fn(cfg_name, frac)
     for _ in range(max(args.warmup, 3)):
         step()
@@ -455,6 +459,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--ref-seconds", type=float, default=60.0,
+                    help="approximate length of the --impl reference run")
     args = ap.parse_args()
     if args.steps is None:
         args.steps = DEFAULT_STEPS[args.config]
