@@ -65,14 +65,29 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+KERNEL_HEADERS = ("kaio_device.cuh", "kaio_internal.h")
+
+
+def kernel_source_sha(kernel_file: str) -> str:
+    """First 16 hex digits of the sha256 over a kernel's source file followed by
+    the device headers every kernel file includes."""
+    csrc = os.path.join(ROOT, "qkv_projection_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in (kernel_file,) + KERNEL_HEADERS:
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
 def profile_traffic(kernel_file: str, config: str):
     """DRAM bytes per launch from the committed ncu summary of this kernel and
     workload, if that summary was taken from the current kernel source."""
-    src = os.path.join(ROOT, "qkv_projection_gb300", "csrc", kernel_file)
+    csrc = os.path.join(ROOT, "qkv_projection_gb300", "csrc")
+    srcs = [os.path.join(csrc, f) for f in (kernel_file,) + KERNEL_HEADERS]
     summary = os.path.join(ROOT, "profiles", f"{config}.md")
-    if not (os.path.exists(src) and os.path.exists(summary)):
+    if not (all(os.path.exists(f) for f in srcs) and os.path.exists(summary)):
         return None
-    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    sha = kernel_source_sha(kernel_file)
     text = open(summary).read()
     m_sha = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]{16})", text)
     m_b = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)

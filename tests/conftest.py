@@ -26,3 +26,13 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+@pytest.fixture(scope="session", autouse=True)
+def _library_built():
+    """Compile the C-ABI library once if it is not there yet (nvcc cross-compiles
+    for sm_103a without a GPU), so host-side tests of the boundary can load it."""
+    from qkv_projection_gb300 import build
+    if not os.path.exists(build.LIB):
+        build.build()
+    yield
