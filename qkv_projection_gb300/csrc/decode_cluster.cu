@@ -72,8 +72,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int XKB = Frag<MT>::kXkb;
   constexpr int F = Frag<MT>::kAcc;
   extern __shared__ unsigned char smem_raw[];
-  unsigned char* smem = reinterpret_cast<unsigned char*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  unsigned char* smem = align_smem_1024(smem_raw);
   __shared__ __align__(8) uint64_t full[kMaxStages], empty[kMaxStages], sbar;
   __shared__ int abort_flag;
 

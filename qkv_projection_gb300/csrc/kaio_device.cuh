@@ -27,6 +27,14 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// First 1024-byte-aligned address at or after p (p in shared memory). The
+// offset is added to p itself, so the compiler still knows the result points
+// into shared memory and emits shared-memory loads and stores through it
+// (rounding the address through an integer would make them generic accesses).
+__device__ __forceinline__ unsigned char* align_smem_1024(unsigned char* p) {
+  return p + ((1024u - (smem_u32(p) & 1023u)) & 1023u);
+}
+
 __device__ __forceinline__ bool elect_lane0() { return (threadIdx.x & 31) == 0; }
 
 // ---------------------------------------------------------------------------

@@ -104,8 +104,7 @@ __global__ void __launch_bounds__(DTHREADS, 1)
                      const __grid_constant__ CUtensorMap tmS0, const __grid_constant__ CUtensorMap tmS1,
                      const __grid_constant__ CUtensorMap tmS2, const DecTcParams p) {
   extern __shared__ unsigned char smem_raw[];
-  unsigned char* smem = reinterpret_cast<unsigned char*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  unsigned char* smem = align_smem_1024(smem_raw);
   __shared__ __align__(8) uint64_t full[DMAX_STAGES], empty[DMAX_STAGES], sbar, a_full[DASTAGES],
       a_empty[DASTAGES], acc_full, mma_done[DMMA_WARPS];
   __shared__ uint32_t tmem_base_sh;
@@ -185,26 +184,18 @@ __global__ void __launch_bounds__(DTHREADS, 1)
   } else if (warp <= DMMA_WARPS) {
     // ------------------------------------------------------------ MMA warps
     // MMA warp w owns the 16-K steps 2w and 2w+1 of each 64-K half of every K
-    // group: when a stage lands it permutes the x chunks of those steps, then
-    // per K group issues their MMAs into its own accumulators D[q][w]. Two
+    // group and issues their MMAs into its own accumulators D[q][w]. Two
     // issuing warps overlap the per-instruction issue cost, which dominates at
-    // N = 16.
+    // N = 16. A group's A stage being full implies its x boxes have landed and
+    // been permuted (the dequant warps do both before their hand-off), so these
+    // warps wait on nothing else.
     const int w = warp - 1;
     constexpr uint32_t idesc = idesc_f16_f32(DN, DM, false, false);
     int a = 0, st = 0;
-    uint32_t aph = 0, ph = 0;
+    uint32_t aph = 0;
     bool ok = true;
     for (int i = 0; i < nstg && ok; ++i) {
-      if (!mbar_wait(&full[st], ph, abort, &g_td_err)) { ok = false; break; }
       unsigned char* sx = smem + st * DSTAGE_BYTES;
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {                // 256 chunks: 4 boxes x 16 rows x 4 chunks
-        const int t = lane * 8 + u;
-        const int b = t >> 6, m = (t >> 2) & 15, c = 4 * w + (t & 3);
-        permute_x_chunk(sx + b * DXBOX + (m >> 3) * 1024 + (m & 7) * 128 + ((c ^ (m & 7)) << 4));
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
       const uint64_t bd0 = sdesc_sw128(smem_u32(sx), 16, 1024);
       const uint32_t blo = static_cast<uint32_t>(bd0), bhi = static_cast<uint32_t>(bd0 >> 32);
       const int ngs = min(DGPS, nsg - i * DGPS);
@@ -231,7 +222,7 @@ __global__ void __launch_bounds__(DTHREADS, 1)
         __syncwarp();
         if (++a == DASTAGES) { a = 0; aph ^= 1; }
       }
-      if (++st == p.nst) { st = 0; ph ^= 1; }
+      if (++st == p.nst) st = 0;
     }
     if (lane == 0) {
       if (ok) umma_commit(&acc_full);              // fires when this warp's MMAs are done
@@ -252,8 +243,17 @@ __global__ void __launch_bounds__(DTHREADS, 1)
     uint32_t aph = 0, ph = 0;
     bool ok = mbar_wait(&sbar, 0, abort, &g_td_err);
     int gl = 0;                                     // group index inside the CTA's range
+    // x chunk this thread permutes in every stage: 4 boxes x 16 rows x 8 chunks
+    // = 512 chunks, one per dequant thread (rows >= M are zeros and stay so).
+    const int pt = threadIdx.x - (1 + DMMA_WARPS) * 32;
+    const int pb = pt >> 7, pm = (pt >> 3) & 15, pc = pt & 7;
+    const int poff = pb * DXBOX + (pm >> 3) * 1024 + (pm & 7) * 128 + ((pc ^ (pm & 7)) << 4);
     for (int i = 0; i < nstg && ok; ++i) {
       if (!mbar_wait(&full[st], ph, abort, &g_td_err)) { ok = false; break; }
+      if (pm < p.M) {
+        permute_x_chunk(smem + st * DSTAGE_BYTES + poff);
+        fence_proxy_async_smem();                 // the MMAs read x through the async proxy
+      }
       const unsigned char* sw = smem + st * DSTAGE_BYTES + DX_STAGE + (2 * qr) * (DN * 4) + nl * 4;
       const int ngs = min(DGPS, nsg - i * DGPS);
       for (int j = 0; j < ngs && ok; ++j, ++gl) {
@@ -303,22 +303,26 @@ __global__ void __launch_bounds__(DTHREADS, 1)
     float* red = reinterpret_cast<float*>(smem);
     const bool have = ok && nsg > 0 && mbar_wait(&acc_full, 0, abort, &g_td_err);
     if (have) tc_fence_after();
+    uint32_t r[3][DMMA_WARPS][4];
+    if (have) {
 #pragma unroll
-    for (int q = 0; q < 3; ++q) {
-      float sum[4] = {0.f, 0.f, 0.f, 0.f};
-      if (have) {
+      for (int q = 0; q < 3; ++q)
 #pragma unroll
-        for (int w2 = 0; w2 < DMMA_WARPS; ++w2) {
-          uint32_t r[4];
-          tmem_ld4(tmem + lane_base + (q * 2 + w2) * DM + qr * 4, r);
-          tmem_ld_wait();
-#pragma unroll
-          for (int jj = 0; jj < 4; ++jj) sum[jj] += __uint_as_float(r[jj]);
-        }
-      }
-#pragma unroll
-      for (int jj = 0; jj < 4; ++jj) red[(q * DM + qr * 4 + jj) * DN + nl] = sum[jj];
+        for (int w2 = 0; w2 < DMMA_WARPS; ++w2)
+          tmem_ld4(tmem + lane_base + (q * 2 + w2) * DM + qr * 4, r[q][w2]);
+      tmem_ld_wait();
     }
+#pragma unroll
+    for (int q = 0; q < 3; ++q)
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) {
+        float sum = 0.f;
+        if (have) {
+#pragma unroll
+          for (int w2 = 0; w2 < DMMA_WARPS; ++w2) sum += __uint_as_float(r[q][w2][jj]);
+        }
+        red[(q * DM + qr * 4 + jj) * DN + nl] = sum;
+      }
     tc_fence_before();
   }
 

@@ -60,8 +60,7 @@ __global__ void __launch_bounds__(GTHREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const GemmParams p) {
   extern __shared__ unsigned char smem_raw[];
-  unsigned char* smem = reinterpret_cast<unsigned char*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  unsigned char* smem = align_smem_1024(smem_raw);
   __shared__ __align__(8) uint64_t full[GSTAGES], empty[GSTAGES], acc_full[2], acc_empty[2],
       mma_done;
   __shared__ uint32_t tmem_base_sh;
@@ -238,8 +237,7 @@ __global__ void __launch_bounds__(PTHREADS, 1)
                     const __grid_constant__ CUtensorMap tmS0, const __grid_constant__ CUtensorMap tmS1,
                     const __grid_constant__ CUtensorMap tmS2, const W4Params p) {
   extern __shared__ unsigned char smem_raw[];
-  unsigned char* smem = reinterpret_cast<unsigned char*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  unsigned char* smem = align_smem_1024(smem_raw);
   __shared__ __align__(8) uint64_t full[PSTAGES], empty[PSTAGES], a_full[2], a_empty[2],
       acc_full, acc_empty, mma_done;
   __shared__ uint32_t tmem_base_sh;
