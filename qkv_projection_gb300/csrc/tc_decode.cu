@@ -14,10 +14,11 @@
 //   (rows >= M are zero-filled by TMA) into a ring of shared-memory stages;
 // * sixteen dequant warps (thread = output column = TMEM lane) turn packed
 //   words into f16 operands in registers and store them into TMEM A stages;
-// * two MMA warps issue tcgen05.mma (A from TMEM, B = x tile from shared
-//   memory) into their own f32 accumulators: at N = 16 the per-instruction
-//   issue cost of one warp would leave the tensor core idle most of the time,
-//   and two issuers overlap it;
+//   they also permute the staged x chunks to the K order of those operands;
+// * three MMA warps, one per projection, issue tcgen05.mma (A from TMEM,
+//   B = x tile from shared memory) into that projection's f32 accumulator: at
+//   N = 16 the per-instruction issue cost of one warp would leave the tensor
+//   core idle most of the time, and three issuers overlap it;
 // * the CTAs of a cluster cover consecutive K ranges of the same 128 columns;
 //   their accumulators are reduced through distributed shared memory, in rank
 //   order (deterministic), and written as f16.
@@ -51,11 +52,11 @@ constexpr int DSTAGE_BYTES = DX_STAGE + 3 * DW_BOX;   // 56 KB, multiple of 1024
 constexpr int DMAX_STAGES = 4;
 constexpr int DSCALE_ROW = 3 * DN * 2;           // the three scale rows of one K group: 768 B
 constexpr int DDQ_WARPS = 16;                    // 4 per TMEM lane quadrant
-constexpr int DMMA_WARPS = 2;                    // each issues half of the 16-K MMA steps
-constexpr int DTHREADS = (1 + DMMA_WARPS + DDQ_WARPS) * 32;   // 608
+constexpr int DMMA_WARPS = 3;                    // one per projection
+constexpr int DTHREADS = (1 + DMMA_WARPS + DDQ_WARPS) * 32;   // 640
 constexpr int DASTAGES = 2;                      // TMEM A stages of one K group (128 K)
 constexpr uint32_t DTMEM_COLS = 512;
-constexpr uint32_t DA_COL0 = 128;                // accumulators D[q][w] at 0..95, A stages after
+constexpr uint32_t DA_COL0 = 64;                 // accumulators D[q] at 0..47, A stages after
 constexpr uint32_t DA_STAGE_COLS = 192;          // 3 projections x 64 columns (128 K)
 constexpr int DRED_BYTES = 3 * DM * DN * 4;      // one CTA's partial tile (24 KB)
 constexpr int DSMEM_LIMIT = 232448 - 1024;       // opt-in per-block limit minus static shared memory
@@ -183,13 +184,14 @@ __global__ void __launch_bounds__(DTHREADS, 1)
     }
   } else if (warp <= DMMA_WARPS) {
     // ------------------------------------------------------------ MMA warps
-    // MMA warp w owns the 16-K steps 2w and 2w+1 of each 64-K half of every K
-    // group and issues their MMAs into its own accumulators D[q][w]. Two
-    // issuing warps overlap the per-instruction issue cost, which dominates at
-    // N = 16. A group's A stage being full implies its x boxes have landed and
-    // been permuted (the dequant warps do both before their hand-off), so these
-    // warps wait on nothing else.
-    const int w = warp - 1;
+    // MMA warp q issues the eight 16-K steps of every K group of projection q
+    // into that projection's accumulator D[q]. At N = 16 the per-instruction
+    // issue cost dominates; three issuing warps overlap it. A group's A stage
+    // being full implies its x boxes have landed and been permuted (the
+    // dequant warps do both before their hand-off), so these warps wait on
+    // nothing else.
+    const int q = warp - 1;
+    const uint32_t dq = tmem + static_cast<uint32_t>(q * DM);
     constexpr uint32_t idesc = idesc_f16_f32(DN, DM, false, false);
     int a = 0, st = 0;
     uint32_t aph = 0;
@@ -204,18 +206,14 @@ __global__ void __launch_bounds__(DTHREADS, 1)
         if (lane == 0) {
           tc_fence_after();
           const uint32_t acc0 = (i | j) != 0 ? 1u : 0u;
+          const uint32_t abase = tmem + DA_COL0 + static_cast<uint32_t>(a * DA_STAGE_COLS + q * 64);
+          const uint32_t xlo = blo + static_cast<uint32_t>((2 * j * DXBOX) >> 4);
 #pragma unroll
           for (int hh = 0; hh < 2; ++hh)
 #pragma unroll
-            for (int k2 = 0; k2 < 2; ++k2) {
-              const int kk = 2 * w + k2;
-              const uint32_t lo = blo + static_cast<uint32_t>(((2 * j + hh) * DXBOX + kk * 32) >> 4);
-#pragma unroll
-              for (int q = 0; q < 3; ++q)
-                umma_ts_lohi(tmem + (q * 2 + w) * DM,
-                             tmem + DA_COL0 + a * DA_STAGE_COLS + q * 64 + kk * 16 + hh * 8, lo, bhi,
-                             idesc, (hh | k2) != 0 ? 1u : acc0);
-            }
+            for (int kk = 0; kk < 4; ++kk)
+              umma_ts_lohi(dq, abase + kk * 16 + hh * 8, xlo + ((hh * DXBOX + kk * 32) >> 4), bhi, idesc,
+                           (hh | kk) != 0 ? 1u : acc0);
           umma_commit(&a_empty[a]);
           if (j == ngs - 1) umma_commit(&empty[st]);
         }
@@ -226,8 +224,8 @@ __global__ void __launch_bounds__(DTHREADS, 1)
     }
     if (lane == 0) {
       if (ok) umma_commit(&acc_full);              // fires when this warp's MMAs are done
-      umma_commit(&mma_done[w]);
-      mbar_wait_drain(&mma_done[w], 0, &g_td_err);
+      umma_commit(&mma_done[q]);
+      mbar_wait_drain(&mma_done[q], 0, &g_td_err);
     }
   } else {
     // ------------------------------------------------------------ dequant warps
@@ -297,32 +295,23 @@ __global__ void __launch_bounds__(DTHREADS, 1)
       if (++st == p.nst) { st = 0; ph ^= 1; }
     }
 
-    // Epilogue part 1: this CTA's partial sum_w D[q][w][n][m] -> shared
+    // Epilogue part 1: this CTA's partial D[q][n][m] -> shared
     // red[q][m][n] (quarter qr drains batch rows 4qr .. 4qr+3). The ring is free
     // once every MMA has completed (acc_full).
     float* red = reinterpret_cast<float*>(smem);
     const bool have = ok && nsg > 0 && mbar_wait(&acc_full, 0, abort, &g_td_err);
     if (have) tc_fence_after();
-    uint32_t r[3][DMMA_WARPS][4];
+    uint32_t r[3][4];
     if (have) {
 #pragma unroll
-      for (int q = 0; q < 3; ++q)
-#pragma unroll
-        for (int w2 = 0; w2 < DMMA_WARPS; ++w2)
-          tmem_ld4(tmem + lane_base + (q * 2 + w2) * DM + qr * 4, r[q][w2]);
+      for (int q = 0; q < 3; ++q) tmem_ld4(tmem + lane_base + q * DM + qr * 4, r[q]);
       tmem_ld_wait();
     }
 #pragma unroll
     for (int q = 0; q < 3; ++q)
 #pragma unroll
-      for (int jj = 0; jj < 4; ++jj) {
-        float sum = 0.f;
-        if (have) {
-#pragma unroll
-          for (int w2 = 0; w2 < DMMA_WARPS; ++w2) sum += __uint_as_float(r[q][w2][jj]);
-        }
-        red[(q * DM + qr * 4 + jj) * DN + nl] = sum;
-      }
+      for (int jj = 0; jj < 4; ++jj)
+        red[(q * DM + qr * 4 + jj) * DN + nl] = have ? __uint_as_float(r[q][jj]) : 0.f;
     tc_fence_before();
   }
 
