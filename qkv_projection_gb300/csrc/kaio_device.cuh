@@ -270,6 +270,15 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32(int m, int n, bool a_mn, bo
 // Mask, sign flip and exponent are one LOP3: (word & mask) ^ magic, where the
 // magic holds the exponent bits and the flipped sign position.
 
+// (a & kMask) ^ magic as one three-input logic instruction (truth table 0x6A).
+// Written out because, left to itself, the compiler spends two logic
+// instructions on this expression when both constants are literals.
+template <uint32_t kMask>
+__device__ __forceinline__ uint32_t and_xor(uint32_t a, uint32_t magic) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(d) : "r"(a), "n"(kMask), "r"(magic));
+  return d;
+}
 __device__ __forceinline__ uint32_t hsub2_rn(uint32_t a, uint32_t b) {
   uint32_t d;
   asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
@@ -299,9 +308,9 @@ struct PairedNibbles {
   __device__ __forceinline__ explicit PairedNibbles(uint32_t word) : w(word), w8(word >> 8) {}
   __device__ __forceinline__ uint32_t pair(int j, uint32_t s2) const {
     const uint32_t src = (j & 2) ? w8 : w;
-    const uint32_t msk = (j & 1) ? kHiMask : kLoMask;
     const uint32_t mag = (j & 1) ? kHiMagic : kLoMagic;
-    return hmul2_rn(hsub2_rn((src & msk) ^ mag, mag), s2);
+    const uint32_t v = (j & 1) ? and_xor<kHiMask>(src, kHiMagic) : and_xor<kLoMask>(src, kLoMagic);
+    return hmul2_rn(hsub2_rn(v, mag), s2);
   }
 };
 
@@ -314,10 +323,10 @@ __device__ __forceinline__ void dequant_natural(uint32_t word, uint32_t s2, uint
   const uint32_t b10 = prmt(word, 0u, 0x0101u);  // bytes {1,0,1,0}
   const uint32_t b23 = prmt(word, 0u, 0x3232u);  // bytes {2,3,2,3}
   const uint32_t b32 = prmt(word, 0u, 0x2323u);  // bytes {3,2,3,2}
-  out[0] = hmul2_rn(hsub2_rn((b01 & kMixMask) ^ kMixMagic, kMixMagic), s2);  // n0, n1
-  out[1] = hmul2_rn(hsub2_rn((b10 & kMixMask) ^ kMixMagic, kMixMagic), s2);  // n2, n3
-  out[2] = hmul2_rn(hsub2_rn((b23 & kMixMask) ^ kMixMagic, kMixMagic), s2);  // n4, n5
-  out[3] = hmul2_rn(hsub2_rn((b32 & kMixMask) ^ kMixMagic, kMixMagic), s2);  // n6, n7
+  out[0] = hmul2_rn(hsub2_rn(and_xor<kMixMask>(b01, kMixMagic), kMixMagic), s2);  // n0, n1
+  out[1] = hmul2_rn(hsub2_rn(and_xor<kMixMask>(b10, kMixMagic), kMixMagic), s2);  // n2, n3
+  out[2] = hmul2_rn(hsub2_rn(and_xor<kMixMask>(b23, kMixMagic), kMixMagic), s2);  // n4, n5
+  out[3] = hmul2_rn(hsub2_rn(and_xor<kMixMask>(b32, kMixMagic), kMixMagic), s2);  // n6, n7
 }
 
 __device__ __forceinline__ uint32_t half2_bits(uint16_t lo, uint16_t hi) {
