@@ -12,7 +12,7 @@
 // * a producer warp streams, per K group of 128 rows, the 16 x 128 packed words
 //   and the scale row of each projection plus two 64-wide 128B-swizzled x boxes
 //   (rows >= M are zero-filled by TMA) into a ring of shared-memory stages;
-// * sixteen dequant warps (thread = output column = TMEM lane) turn packed
+// * eight dequant warps (thread = output column = TMEM lane) turn packed
 //   words into f16 operands in registers and store them into TMEM A stages;
 //   they also permute the staged x chunks to the K order of those operands;
 // * three MMA warps, one per projection, issue tcgen05.mma (A from TMEM,
@@ -51,9 +51,9 @@ constexpr int DW_BOX = DGPS * 16 * DN * 4;       // 32 packed rows x 128 columns
 constexpr int DSTAGE_BYTES = DX_STAGE + 3 * DW_BOX;   // 56 KB, multiple of 1024
 constexpr int DMAX_STAGES = 4;
 constexpr int DSCALE_ROW = 3 * DN * 2;           // the three scale rows of one K group: 768 B
-constexpr int DDQ_WARPS = 16;                    // 4 per TMEM lane quadrant
+constexpr int DDQ_WARPS = 8;                     // 2 per TMEM lane quadrant
 constexpr int DMMA_WARPS = 3;                    // one per projection
-constexpr int DTHREADS = (1 + DMMA_WARPS + DDQ_WARPS) * 32;   // 640
+constexpr int DTHREADS = (1 + DMMA_WARPS + DDQ_WARPS) * 32;   // 384
 constexpr int DASTAGES = 2;                      // TMEM A stages of one K group (128 K)
 constexpr uint32_t DTMEM_COLS = 512;
 constexpr uint32_t DA_COL0 = 64;                 // accumulators D[q] at 0..47, A stages after
@@ -229,11 +229,12 @@ __global__ void __launch_bounds__(DTHREADS, 1)
     }
   } else {
     // ------------------------------------------------------------ dequant warps
-    // Thread = output column n0 + 32*sp + lane = TMEM lane. Quarter qr fills
-    // the 16-K MMA step qr of both 64-K halves of each K group (packed rows
-    // 2qr, 2qr+1 and 8+2qr, 9+2qr): 16 TMEM columns per projection, one store.
+    // Thread = output column n0 + 32*sp + lane = TMEM lane. Half hq fills the
+    // 16-K MMA steps 2hq and 2hq+1 of both 64-K halves of each K group (packed
+    // rows 4hq..4hq+3 and 8+4hq..8+4hq+3): 32 consecutive TMEM columns per
+    // projection, one store each.
     const int sp = warp & 3;
-    const int qr = (warp - 1 - DMMA_WARPS) >> 2;
+    const int hq = (warp - 1 - DMMA_WARPS) >> 2;
     const int nl = 32 * sp + lane;
     const uint32_t lane_base = static_cast<uint32_t>(32 * sp) << 16;
     const unsigned char* scale_base = smem + p.s_off + nl * 2;
@@ -241,8 +242,10 @@ __global__ void __launch_bounds__(DTHREADS, 1)
     uint32_t aph = 0, ph = 0;
     bool ok = mbar_wait(&sbar, 0, abort, &g_td_err);
     int gl = 0;                                     // group index inside the CTA's range
-    // x chunk this thread permutes in every stage: 4 boxes x 16 rows x 8 chunks
-    // = 512 chunks, one per dequant thread (rows >= M are zeros and stay so).
+    // x chunks this thread permutes in every stage: 4 boxes x 16 rows x 8
+    // chunks = 512 chunks, two per dequant thread (rows >= M are zeros and
+    // stay so): chunk pt and pt + 256, i.e. the same row and chunk of boxes
+    // pb and pb + 2.
     const int pt = threadIdx.x - (1 + DMMA_WARPS) * 32;
     const int pb = pt >> 7, pm = (pt >> 3) & 15, pc = pt & 7;
     const int poff = pb * DXBOX + (pm >> 3) * 1024 + (pm & 7) * 128 + ((pc ^ (pm & 7)) << 4);
@@ -250,23 +253,26 @@ __global__ void __launch_bounds__(DTHREADS, 1)
       if (!mbar_wait(&full[st], ph, abort, &g_td_err)) { ok = false; break; }
       if (pm < p.M) {
         permute_x_chunk(smem + st * DSTAGE_BYTES + poff);
+        permute_x_chunk(smem + st * DSTAGE_BYTES + poff + 2 * DXBOX);
         fence_proxy_async_smem();                 // the MMAs read x through the async proxy
       }
-      const unsigned char* sw = smem + st * DSTAGE_BYTES + DX_STAGE + (2 * qr) * (DN * 4) + nl * 4;
+      const unsigned char* sw = smem + st * DSTAGE_BYTES + DX_STAGE + (4 * hq) * (DN * 4) + nl * 4;
       const int ngs = min(DGPS, nsg - i * DGPS);
       for (int j = 0; j < ngs && ok; ++j, ++gl) {
         // scale rows of group gl: box gl/8 (boxes hold up to 8 rows), row gl%8
         const unsigned char* sc = scale_base + (gl >> 3) * p.sbox * DSCALE_ROW + (gl & 7) * (DN * 2);
-        uint32_t wd[3][4], s2[3];
+        // wd[q][hh*4 + r] = packed row hh*8 + 4hq + r (r = 0..3)
+        uint32_t wd[3][8], s2[3];
 #pragma unroll
         for (int q = 0; q < 3; ++q) {
           const uint16_t sb = *reinterpret_cast<const uint16_t*>(sc + q * p.sbox * DN * 2);
           s2[q] = half2_bits(sb, sb);
           const unsigned char* wq = sw + q * DW_BOX + j * 16 * (DN * 4);
-          wd[q][0] = *reinterpret_cast<const uint32_t*>(wq);
-          wd[q][1] = *reinterpret_cast<const uint32_t*>(wq + DN * 4);
-          wd[q][2] = *reinterpret_cast<const uint32_t*>(wq + 8 * DN * 4);
-          wd[q][3] = *reinterpret_cast<const uint32_t*>(wq + 9 * DN * 4);
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+              wd[q][hh * 4 + r] = *reinterpret_cast<const uint32_t*>(wq + (hh * 8 + r) * (DN * 4));
         }
         if (j == ngs - 1) {
           __syncwarp();
@@ -274,17 +280,23 @@ __global__ void __launch_bounds__(DTHREADS, 1)
         }
         if (!mbar_wait(&a_empty[a], aph ^ 1, abort, &g_td_err)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t tbase = tmem + lane_base + DA_COL0 + a * DA_STAGE_COLS + qr * 16;
+        const uint32_t tbase = tmem + lane_base + DA_COL0 + a * DA_STAGE_COLS + hq * 32;
 #pragma unroll
         for (int q = 0; q < 3; ++q) {
-          uint32_t v[16];
+          // column (kk - 2hq)*16 + hh*8 + 4*rr + jj of this thread's 32 holds
+          // K pair jj of packed row hh*8 + 2*kk + rr (the A layout of an MMA step)
+          uint32_t v[32];
 #pragma unroll
-          for (int r = 0; r < 4; ++r) {
-            const PairedNibbles pn(wd[q][r]);
+          for (int k2 = 0; k2 < 2; ++k2)
 #pragma unroll
-            for (int jj = 0; jj < 4; ++jj) v[4 * r + jj] = pn.pair(jj, s2[q]);
-          }
-          tmem_st16(tbase + q * 64, v);
+            for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+              for (int rr = 0; rr < 2; ++rr) {
+                const PairedNibbles pn(wd[q][hh * 4 + 2 * k2 + rr]);
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) v[k2 * 16 + hh * 8 + 4 * rr + jj] = pn.pair(jj, s2[q]);
+              }
+          tmem_st32(tbase + q * 64, v);
         }
         tmem_st_wait();
         tc_fence_before();
@@ -296,22 +308,22 @@ __global__ void __launch_bounds__(DTHREADS, 1)
     }
 
     // Epilogue part 1: this CTA's partial D[q][n][m] -> shared
-    // red[q][m][n] (quarter qr drains batch rows 4qr .. 4qr+3). The ring is free
+    // red[q][m][n] (half hq drains batch rows 8hq .. 8hq+7). The ring is free
     // once every MMA has completed (acc_full).
     float* red = reinterpret_cast<float*>(smem);
     const bool have = ok && nsg > 0 && mbar_wait(&acc_full, 0, abort, &g_td_err);
     if (have) tc_fence_after();
-    uint32_t r[3][4];
+    uint32_t r[3][8];
     if (have) {
 #pragma unroll
-      for (int q = 0; q < 3; ++q) tmem_ld4(tmem + lane_base + q * DM + qr * 4, r[q]);
+      for (int q = 0; q < 3; ++q) tmem_ld8(tmem + lane_base + q * DM + hq * 8, r[q]);
       tmem_ld_wait();
     }
 #pragma unroll
     for (int q = 0; q < 3; ++q)
 #pragma unroll
-      for (int jj = 0; jj < 4; ++jj)
-        red[(q * DM + qr * 4 + jj) * DN + nl] = have ? __uint_as_float(r[q][jj]) : 0.f;
+      for (int jj = 0; jj < 8; ++jj)
+        red[(q * DM + hq * 8 + jj) * DN + nl] = have ? __uint_as_float(r[q][jj]) : 0.f;
     tc_fence_before();
   }
 
