@@ -91,13 +91,18 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
                                           unsigned* err) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
-  for (;;) {
+  for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait_sleep(bar, parity)) return true;
-    if (*abort) return false;
-    if (globaltimer() - t0 > kWaitLimitNs) {
-      *abort = 1;
-      atomicOr(err, kDevErrTimeout);
-      return false;
+    // The abort flag and the clock are looked at every 64th try only: a try
+    // that fails costs the waiting warp a few instructions, and waiting warps
+    // share their scheduler with warps doing the dequant arithmetic.
+    if ((it & 63u) == 0) {
+      if (*abort) return false;
+      if (globaltimer() - t0 > kWaitLimitNs) {
+        *abort = 1;
+        atomicOr(err, kDevErrTimeout);
+        return false;
+      }
     }
   }
 }

@@ -127,7 +127,7 @@ __global__ void __launch_bounds__(DTHREADS, 1)
     }
     mbar_init(&sbar, 1);
     for (int a = 0; a < DASTAGES; ++a) {
-      mbar_init(&a_full[a], DDQ_WARPS);
+      mbar_init(&a_full[a], DDQ_WARPS / 2);       // the set of dequant warps owning stage a
       mbar_init(&a_empty[a], DMMA_WARPS);
     }
     mbar_init(&acc_full, DMMA_WARPS);
@@ -229,86 +229,88 @@ __global__ void __launch_bounds__(DTHREADS, 1)
     }
   } else {
     // ------------------------------------------------------------ dequant warps
-    // Thread = output column n0 + 32*sp + lane = TMEM lane. Half hq fills the
-    // 16-K MMA steps 2hq and 2hq+1 of both 64-K halves of each K group (packed
-    // rows 4hq..4hq+3 and 8+4hq..8+4hq+3): 32 consecutive TMEM columns per
-    // projection, one store each.
+    // Two sets of four warps (one per TMEM lane quadrant). Set js takes the
+    // K groups with j == js in every shared-memory stage (even / odd groups)
+    // and owns TMEM A stage js, so each set waits only for the MMAs of its
+    // own previous group: the sets drift out of phase and one set's waits and
+    // loads overlap the other set's arithmetic. Thread = output column
+    // n0 + 32*sp + lane = TMEM lane; it dequantises all 16 packed rows of its
+    // column for the three projections (48 words per group).
     const int sp = warp & 3;
-    const int hq = (warp - 1 - DMMA_WARPS) >> 2;
+    const int js = (warp - 1 - DMMA_WARPS) >> 2;
     const int nl = 32 * sp + lane;
     const uint32_t lane_base = static_cast<uint32_t>(32 * sp) << 16;
     const unsigned char* scale_base = smem + p.s_off + nl * 2;
-    int a = 0, st = 0;
+    int st = 0;
     uint32_t aph = 0, ph = 0;
     bool ok = mbar_wait(&sbar, 0, abort, &g_td_err);
-    int gl = 0;                                     // group index inside the CTA's range
-    // x chunks this thread permutes in every stage: 4 boxes x 16 rows x 8
-    // chunks = 512 chunks, two per dequant thread (rows >= M are zeros and
-    // stay so): chunk pt and pt + 256, i.e. the same row and chunk of boxes
-    // pb and pb + 2.
-    const int pt = threadIdx.x - (1 + DMMA_WARPS) * 32;
-    const int pb = pt >> 7, pm = (pt >> 3) & 15, pc = pt & 7;
-    const int poff = pb * DXBOX + (pm >> 3) * 1024 + (pm & 7) * 128 + ((pc ^ (pm & 7)) << 4);
+    // x chunks this thread permutes in its groups: the two 64-K boxes 2js and
+    // 2js+1 of a group hold 2 x 16 rows x 8 chunks = 256 chunks, two per
+    // thread of the set (rows >= M are zeros and stay so).
+    const int pt = (threadIdx.x - (1 + DMMA_WARPS) * 32) & 127;
+    const int pm = (pt >> 3) & 15, pc = pt & 7;
+    const int poff = 2 * js * DXBOX + (pm >> 3) * 1024 + (pm & 7) * 128 + ((pc ^ (pm & 7)) << 4);
+    const uint32_t tbase = tmem + lane_base + DA_COL0 + js * DA_STAGE_COLS;
     for (int i = 0; i < nstg && ok; ++i) {
-      if (!mbar_wait(&full[st], ph, abort, &g_td_err)) { ok = false; break; }
-      if (pm < p.M) {
-        permute_x_chunk(smem + st * DSTAGE_BYTES + poff);
-        permute_x_chunk(smem + st * DSTAGE_BYTES + poff + 2 * DXBOX);
-        fence_proxy_async_smem();                 // the MMAs read x through the async proxy
-      }
-      const unsigned char* sw = smem + st * DSTAGE_BYTES + DX_STAGE + (4 * hq) * (DN * 4) + nl * 4;
       const int ngs = min(DGPS, nsg - i * DGPS);
-      for (int j = 0; j < ngs && ok; ++j, ++gl) {
+      if (js < ngs) {
+        if (!mbar_wait(&full[st], ph, abort, &g_td_err)) { ok = false; break; }
+        if (pm < p.M) {
+          permute_x_chunk(smem + st * DSTAGE_BYTES + poff);
+          permute_x_chunk(smem + st * DSTAGE_BYTES + poff + DXBOX);
+          fence_proxy_async_smem();               // the MMAs read x through the async proxy
+        }
+        const int gl = i * DGPS + js;             // group index inside the CTA's range
         // scale rows of group gl: box gl/8 (boxes hold up to 8 rows), row gl%8
         const unsigned char* sc = scale_base + (gl >> 3) * p.sbox * DSCALE_ROW + (gl & 7) * (DN * 2);
-        // wd[q][hh*4 + r] = packed row hh*8 + 4hq + r (r = 0..3)
-        uint32_t wd[3][8], s2[3];
+        const unsigned char* sw = smem + st * DSTAGE_BYTES + DX_STAGE + js * 16 * (DN * 4) + nl * 4;
+        uint32_t wd[3][16], s2[3];                // wd[q][row]: packed rows 0..15 of the group
 #pragma unroll
         for (int q = 0; q < 3; ++q) {
           const uint16_t sb = *reinterpret_cast<const uint16_t*>(sc + q * p.sbox * DN * 2);
           s2[q] = half2_bits(sb, sb);
-          const unsigned char* wq = sw + q * DW_BOX + j * 16 * (DN * 4);
 #pragma unroll
-          for (int hh = 0; hh < 2; ++hh)
-#pragma unroll
-            for (int r = 0; r < 4; ++r)
-              wd[q][hh * 4 + r] = *reinterpret_cast<const uint32_t*>(wq + (hh * 8 + r) * (DN * 4));
+          for (int r = 0; r < 16; ++r)
+            wd[q][r] = *reinterpret_cast<const uint32_t*>(sw + q * DW_BOX + r * (DN * 4));
         }
-        if (j == ngs - 1) {
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&empty[st]);   // packed words of this stage are in registers
-        }
-        if (!mbar_wait(&a_empty[a], aph ^ 1, abort, &g_td_err)) { ok = false; break; }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[st]);   // this set's words of the stage are in registers
+        if (!mbar_wait(&a_empty[js], aph ^ 1, abort, &g_td_err)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t tbase = tmem + lane_base + DA_COL0 + a * DA_STAGE_COLS + hq * 32;
 #pragma unroll
-        for (int q = 0; q < 3; ++q) {
-          // column (kk - 2hq)*16 + hh*8 + 4*rr + jj of this thread's 32 holds
-          // K pair jj of packed row hh*8 + 2*kk + rr (the A layout of an MMA step)
-          uint32_t v[32];
+        for (int q = 0; q < 3; ++q)
 #pragma unroll
-          for (int k2 = 0; k2 < 2; ++k2)
+          for (int k2 = 0; k2 < 2; ++k2) {
+            // column kk*16 + hh*8 + 4*rr + jj (kk = 2*k2 + kx) of projection q's 64
+            // holds K pair jj of packed row hh*8 + 2*kk + rr (the A layout of an MMA
+            // step); one 32-column store covers MMA steps 2*k2 and 2*k2+1
+            uint32_t v[32];
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh)
+            for (int kx = 0; kx < 2; ++kx)
 #pragma unroll
-              for (int rr = 0; rr < 2; ++rr) {
-                const PairedNibbles pn(wd[q][hh * 4 + 2 * k2 + rr]);
+              for (int hh = 0; hh < 2; ++hh)
 #pragma unroll
-                for (int jj = 0; jj < 4; ++jj) v[k2 * 16 + hh * 8 + 4 * rr + jj] = pn.pair(jj, s2[q]);
-              }
-          tmem_st32(tbase + q * 64, v);
-        }
+                for (int rr = 0; rr < 2; ++rr) {
+                  const PairedNibbles pn(wd[q][hh * 8 + 2 * (2 * k2 + kx) + rr]);
+#pragma unroll
+                  for (int jj = 0; jj < 4; ++jj) v[kx * 16 + hh * 8 + 4 * rr + jj] = pn.pair(jj, s2[q]);
+                }
+            tmem_st32(tbase + q * 64 + k2 * 32, v);
+          }
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&a_full[a]);
-        if (++a == DASTAGES) { a = 0; aph ^= 1; }
+        if (lane == 0) mbar_arrive(&a_full[js]);
+        aph ^= 1;
+      } else {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[st]);   // no group of this set in the CTA's last stage
       }
       if (++st == p.nst) { st = 0; ph ^= 1; }
     }
 
     // Epilogue part 1: this CTA's partial D[q][n][m] -> shared
-    // red[q][m][n] (half hq drains batch rows 8hq .. 8hq+7). The ring is free
+    // red[q][m][n] (set js drains batch rows 8js .. 8js+7). The ring is free
     // once every MMA has completed (acc_full).
     float* red = reinterpret_cast<float*>(smem);
     const bool have = ok && nsg > 0 && mbar_wait(&acc_full, 0, abort, &g_td_err);
@@ -316,14 +318,14 @@ __global__ void __launch_bounds__(DTHREADS, 1)
     uint32_t r[3][8];
     if (have) {
 #pragma unroll
-      for (int q = 0; q < 3; ++q) tmem_ld8(tmem + lane_base + q * DM + hq * 8, r[q]);
+      for (int q = 0; q < 3; ++q) tmem_ld8(tmem + lane_base + q * DM + js * 8, r[q]);
       tmem_ld_wait();
     }
 #pragma unroll
     for (int q = 0; q < 3; ++q)
 #pragma unroll
       for (int jj = 0; jj < 8; ++jj)
-        red[(q * DM + hq * 8 + jj) * DN + nl] = have ? __uint_as_float(r[q][jj]) : 0.f;
+        red[(q * DM + js * 8 + jj) * DN + nl] = have ? __uint_as_float(r[q][jj]) : 0.f;
     tc_fence_before();
   }
 
