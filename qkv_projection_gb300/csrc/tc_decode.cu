@@ -106,7 +106,7 @@ __global__ void __launch_bounds__(DTHREADS, 1)
                      const __grid_constant__ CUtensorMap tmS2, const DecTcParams p) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = align_smem_1024(smem_raw);
-  __shared__ __align__(8) uint64_t full[DMAX_STAGES], empty[DMAX_STAGES], sbar, a_full[DASTAGES],
+  __shared__ __align__(8) uint64_t full[DMAX_STAGES], empty[DMAX_STAGES], sbar0, sbar, a_full[DASTAGES],
       a_empty[DASTAGES], acc_full, mma_done[DMMA_WARPS];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
@@ -120,11 +120,44 @@ __global__ void __launch_bounds__(DTHREADS, 1)
   const int nstg = (nsg + DGPS - 1) / DGPS;              // shared-memory stages of this CTA
   volatile int* abort = &abort_flag;
 
+  // Producer state (thread 0). The first copies are issued before the TMEM
+  // allocation and the block barrier so that their latency overlaps the
+  // set-up, in the order the consumers need them: stage 0, the first box of
+  // scale rows, stage 1, the other scale boxes; the rest of the ring follows
+  // once stage 0 has landed (every SM asks for its first stages at the same
+  // moment, and copies issued together land together).
+  uint32_t fills[DMAX_STAGES] = {0, 0, 0, 0};
+  int pst = 0, pi = 0;
+  uint32_t pph = 0;
+  const int nsb = (nsg + p.sbox - 1) / p.sbox;             // boxes of scale rows
+  auto issue_stage = [&]() {
+    unsigned char* sx = smem + pst * DSTAGE_BYTES;
+    unsigned char* sw = sx + DX_STAGE;
+    const int g = g_begin + pi * DGPS;
+    mbar_arrive_expect_tx(&full[pst], DSTAGE_BYTES);
+    tma_load_2d(sw, &tmW0, &full[pst], n0, g * 16);
+    tma_load_2d(sw + DW_BOX, &tmW1, &full[pst], n0, g * 16);
+    tma_load_2d(sw + 2 * DW_BOX, &tmW2, &full[pst], n0, g * 16);
+#pragma unroll
+    for (int b = 0; b < 2 * DGPS; ++b)
+      tma_load_2d(sx + b * DXBOX, &tmX, &full[pst], (g * 2 + b) * 64, 0);
+    ++fills[pst];
+    ++pi;
+    if (++pst == p.nst) { pst = 0; pph ^= 1; }
+  };
+  auto issue_scales = [&](int b, uint64_t* bar) {
+    unsigned char* ss = smem + p.s_off + b * p.sbox * DSCALE_ROW;
+    tma_load_2d(ss, &tmS0, bar, n0, g_begin + b * p.sbox);
+    tma_load_2d(ss + p.sbox * DN * 2, &tmS1, bar, n0, g_begin + b * p.sbox);
+    tma_load_2d(ss + 2 * p.sbox * DN * 2, &tmS2, bar, n0, g_begin + b * p.sbox);
+  };
+
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.nst; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], DDQ_WARPS + DMMA_WARPS);   // dequant warps + one commit per MMA warp
     }
+    mbar_init(&sbar0, 1);
     mbar_init(&sbar, 1);
     for (int a = 0; a < DASTAGES; ++a) {
       mbar_init(&a_full[a], DDQ_WARPS / 2);       // the set of dequant warps owning stage a
@@ -134,6 +167,19 @@ __global__ void __launch_bounds__(DTHREADS, 1)
     for (int w = 0; w < DMMA_WARPS; ++w) mbar_init(&mma_done[w], 1);
     abort_flag = 0;
     fence_mbar_init();
+    tma_prefetch_desc(&tmX);
+    tma_prefetch_desc(&tmW0); tma_prefetch_desc(&tmW1); tma_prefetch_desc(&tmW2);
+    tma_prefetch_desc(&tmS0); tma_prefetch_desc(&tmS1); tma_prefetch_desc(&tmS2);
+    if (nstg > 0) issue_stage();
+    if (nsb > 0) {
+      mbar_arrive_expect_tx(&sbar0, static_cast<uint32_t>(3 * p.sbox * DN * 2));
+      issue_scales(0, &sbar0);
+    }
+    if (pi < nstg && pi < p.nst) issue_stage();
+    if (nsb > 1) {
+      mbar_arrive_expect_tx(&sbar, static_cast<uint32_t>(3 * (nsb - 1) * p.sbox * DN * 2));
+      for (int b = 1; b < nsb; ++b) issue_scales(b, &sbar);
+    }
   }
   if (warp == 0) {
     tmem_alloc(&tmem_base_sh, DTMEM_COLS);
@@ -147,40 +193,19 @@ __global__ void __launch_bounds__(DTHREADS, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     // Few, large copies: per stage one 16 KB box of packed words per projection
-    // and four 2 KB x boxes; the scale rows of the whole K range up front.
+    // and four 2 KB x boxes; the scale rows of the whole K range (issued above
+    // with the first two stages).
     if (lane == 0) {
-      tma_prefetch_desc(&tmX);
-      tma_prefetch_desc(&tmW0); tma_prefetch_desc(&tmW1); tma_prefetch_desc(&tmW2);
-      tma_prefetch_desc(&tmS0); tma_prefetch_desc(&tmS1); tma_prefetch_desc(&tmS2);
-      const int nsb = (nsg + p.sbox - 1) / p.sbox;
-      mbar_arrive_expect_tx(&sbar, static_cast<uint32_t>(3 * nsb * p.sbox * DN * 2));
-      for (int b = 0; b < nsb; ++b) {
-        unsigned char* ss = smem + p.s_off + b * p.sbox * DSCALE_ROW;
-        tma_load_2d(ss, &tmS0, &sbar, n0, g_begin + b * p.sbox);
-        tma_load_2d(ss + p.sbox * DN * 2, &tmS1, &sbar, n0, g_begin + b * p.sbox);
-        tma_load_2d(ss + 2 * p.sbox * DN * 2, &tmS2, &sbar, n0, g_begin + b * p.sbox);
-      }
-      uint32_t fills[DMAX_STAGES] = {0, 0, 0, 0};
-      int st = 0;
-      uint32_t ph = 0;
-      for (int i = 0; i < nstg; ++i) {
-        if (i >= p.nst && !mbar_wait(&empty[st], ph ^ 1, abort, &g_td_err)) break;
-        ++fills[st];
-        unsigned char* sx = smem + st * DSTAGE_BYTES;
-        unsigned char* sw = sx + DX_STAGE;
-        const int g = g_begin + i * DGPS;
-        mbar_arrive_expect_tx(&full[st], DSTAGE_BYTES);
-        tma_load_2d(sw, &tmW0, &full[st], n0, g * 16);
-        tma_load_2d(sw + DW_BOX, &tmW1, &full[st], n0, g * 16);
-        tma_load_2d(sw + 2 * DW_BOX, &tmW2, &full[st], n0, g * 16);
-#pragma unroll
-        for (int b = 0; b < 2 * DGPS; ++b)
-          tma_load_2d(sx + b * DXBOX, &tmX, &full[st], (g * 2 + b) * 64, 0);
-        if (++st == p.nst) { st = 0; ph ^= 1; }
+      bool ok = pi >= nstg || pi >= p.nst || mbar_wait(&full[0], 0, abort, &g_td_err);
+      while (ok && pi < nstg && pi < p.nst) issue_stage();   // the rest of the first ring
+      while (ok && pi < nstg) {
+        if (!mbar_wait(&empty[pst], pph ^ 1, abort, &g_td_err)) break;
+        issue_stage();
       }
       for (int s2 = 0; s2 < p.nst; ++s2)
         if (fills[s2]) mbar_wait_drain(&full[s2], (fills[s2] - 1) & 1, &g_td_err);
-      mbar_wait_drain(&sbar, 0, &g_td_err);
+      if (nsb > 0) mbar_wait_drain(&sbar0, 0, &g_td_err);
+      if (nsb > 1) mbar_wait_drain(&sbar, 0, &g_td_err);
     }
   } else if (warp <= DMMA_WARPS) {
     // ------------------------------------------------------------ MMA warps
@@ -243,7 +268,8 @@ __global__ void __launch_bounds__(DTHREADS, 1)
     const unsigned char* scale_base = smem + p.s_off + nl * 2;
     int st = 0;
     uint32_t aph = 0, ph = 0;
-    bool ok = mbar_wait(&sbar, 0, abort, &g_td_err);
+    bool ok = nsb == 0 || mbar_wait(&sbar0, 0, abort, &g_td_err);
+    bool have_scales = nsb <= 1;                 // rows of the later scale boxes have landed
     // x chunks this thread permutes in its groups: the two 64-K boxes 2js and
     // 2js+1 of a group hold 2 x 16 rows x 8 chunks = 256 chunks, two per
     // thread of the set (rows >= M are zeros and stay so).
@@ -261,6 +287,10 @@ __global__ void __launch_bounds__(DTHREADS, 1)
           fence_proxy_async_smem();               // the MMAs read x through the async proxy
         }
         const int gl = i * DGPS + js;             // group index inside the CTA's range
+        if (!have_scales && gl >= p.sbox) {
+          if (!mbar_wait(&sbar, 0, abort, &g_td_err)) { ok = false; break; }
+          have_scales = true;
+        }
         // scale rows of group gl: box gl/8 (boxes hold up to 8 rows), row gl%8
         const unsigned char* sc = scale_base + (gl >> 3) * p.sbox * DSCALE_ROW + (gl & 7) * (DN * 2);
         const unsigned char* sw = smem + st * DSTAGE_BYTES + DX_STAGE + js * 16 * (DN * 4) + nl * 4;
