@@ -305,17 +305,22 @@ __global__ void __launch_bounds__(PTHREADS, 1)
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_f16_f32(PBN, PBM, false, false);
       int st = 0, a = 0;
-      uint32_t ph = 0, aph = 0, cph = 0;
+      uint32_t aph = 0, cph = 0;
+      bool ahead = false;          // the current A stage was seen full by a look-ahead test
       for (int tile = blockIdx.x; tile < p.tiles; tile += gridDim.x) {
         if (!mbar_wait(&acc_empty, cph ^ 1, abort, &g_tc_err)) break;
         tc_fence_after();
         bool ok = true;
         for (int ks = 0; ks < nks && ok; ++ks) {
-          if (!mbar_wait(&full[st], ph, abort, &g_tc_err)) { ok = false; break; }
+          // No wait on the stage itself: an A stage is full only after the
+          // dequant warps have waited for this stage, so it has landed.
           const uint32_t sx = smem_u32(smem + st * PSTAGE_BYTES);
           for (int hh = 0; hh < 2; ++hh) {
-            if (!mbar_wait(&a_full[a], aph, abort, &g_tc_err)) { ok = false; break; }
+            if (!ahead && !mbar_wait(&a_full[a], aph, abort, &g_tc_err)) { ok = false; break; }
             tc_fence_after();
+            // Test the next A stage now; the test's latency overlaps this
+            // stage's MMA issue, and a stage already full needs no wait.
+            ahead = mbar_test_wait(&a_full[a ^ 1], a == 1 ? aph ^ 1 : aph);
 #pragma unroll
             for (int q = 0; q < 3; ++q) {
 #pragma unroll
@@ -330,7 +335,7 @@ __global__ void __launch_bounds__(PTHREADS, 1)
           }
           if (!ok) break;
           umma_commit(&empty[st]);
-          if (++st == PSTAGES) { st = 0; ph ^= 1; }
+          if (++st == PSTAGES) st = 0;
         }
         if (!ok) break;
         umma_commit(&acc_full);
