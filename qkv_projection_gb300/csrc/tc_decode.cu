@@ -89,16 +89,6 @@ __device__ __forceinline__ void permute_x_chunk(unsigned char* p) {
   *reinterpret_cast<uint4*>(p) = o;
 }
 
-// tcgen05.mma kind::f16, A from TMEM, B descriptor given as two 32-bit halves.
-__device__ __forceinline__ void umma_ts_lohi(uint32_t d, uint32_t a, uint32_t lo, uint32_t hi,
-                                             uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t.reg .b64 bd;\n\tsetp.ne.b32 p, %5, 0;\n\tmov.b64 bd, {%2, %3};\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], bd, %4, p;\n\t}" ::"r"(d),
-      "r"(a), "r"(lo), "r"(hi), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
 __global__ void __launch_bounds__(DTHREADS, 1)
     tc_decode_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW0,
                      const __grid_constant__ CUtensorMap tmW1, const __grid_constant__ CUtensorMap tmW2,

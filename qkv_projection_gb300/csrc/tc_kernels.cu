@@ -314,7 +314,8 @@ __global__ void __launch_bounds__(PTHREADS, 1)
         for (int ks = 0; ks < nks && ok; ++ks) {
           // No wait on the stage itself: an A stage is full only after the
           // dequant warps have waited for this stage, so it has landed.
-          const uint32_t sx = smem_u32(smem + st * PSTAGE_BYTES);
+          const uint64_t bd0 = sdesc_sw128(smem_u32(smem + st * PSTAGE_BYTES), 16, 1024);
+          const uint32_t blo = static_cast<uint32_t>(bd0), bhi = static_cast<uint32_t>(bd0 >> 32);
           for (int hh = 0; hh < 2; ++hh) {
             if (!ahead && !mbar_wait(&a_full[a], aph, abort, &g_tc_err)) { ok = false; break; }
             tc_fence_after();
@@ -326,8 +327,8 @@ __global__ void __launch_bounds__(PTHREADS, 1)
 #pragma unroll
               for (int kk = 0; kk < 2; ++kk) {
                 const uint32_t at = tmem + PA_COL0 + a * PA_STAGE_COLS + q * 16 + kk * 8;
-                const uint64_t bd = sdesc_sw128(sx + (2 * hh + kk) * 32, 16, 1024);
-                umma_ts(tmem + q * PBM, at, bd, idesc, (ks | hh | kk) != 0 ? 1u : 0u);
+                umma_ts_lohi(tmem + q * PBM, at, blo + (((2 * hh + kk) * 32) >> 4), bhi, idesc,
+                             (ks | hh | kk) != 0 ? 1u : 0u);
               }
             }
             umma_commit(&a_empty[a]);
