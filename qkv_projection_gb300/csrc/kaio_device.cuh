@@ -134,6 +134,20 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, 
 }
 
 // ---------------------------------------------------------------------------
+// Programmatic dependent launch. A kernel launched with programmatic stream
+// serialization may start before the previous kernel in its stream has
+// finished; grid_dependency_wait() returns once that kernel has completed and
+// its memory operations are visible, so every thread runs it before its first
+// global-memory access. allow_dependents_launch() lets the next such kernel
+// start its CTAs (on free SMs) once every CTA of this grid has signalled.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void allow_dependents_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
 // TMA (tiled tensor copies global -> shared, completion on an mbarrier)
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");

@@ -157,6 +157,7 @@ __global__ void __launch_bounds__(DTHREADS, 1)
     for (int w = 0; w < DMMA_WARPS; ++w) mbar_init(&mma_done[w], 1);
     abort_flag = 0;
     fence_mbar_init();
+    grid_dependency_wait();                       // the previous kernel's writes are visible
     tma_prefetch_desc(&tmX);
     tma_prefetch_desc(&tmW0); tma_prefetch_desc(&tmW1); tma_prefetch_desc(&tmW2);
     tma_prefetch_desc(&tmS0); tma_prefetch_desc(&tmS1); tma_prefetch_desc(&tmS2);
@@ -179,6 +180,8 @@ __global__ void __launch_bounds__(DTHREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
+  grid_dependency_wait();                         // returns at once: thread 0 has waited
+  allow_dependents_launch();
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -491,13 +494,18 @@ cudaError_t launch_tc_decode(const __half* x, const uint32_t* const w[3], const 
   // and must be alone on its SM.
   cfg.dynamicSmemBytes = std::max(smem_used, static_cast<size_t>(120 * 1024));
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  // Programmatic stream serialization: the next call's CTAs may start (and set
+  // up) on free SMs before this one ends; each waits for its predecessor with
+  // grid_dependency_wait() before touching global memory.
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = static_cast<unsigned>(pl.S);
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   e = cudaLaunchKernelEx(&cfg, tc_decode_kernel, tx, tw[0], tw[1], tw[2], ts[0], ts[1], ts[2], p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
