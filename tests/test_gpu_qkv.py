@@ -173,3 +173,41 @@ def test_decode_shared_memory_sizes_in_any_order():
 
 def test_no_device_timeouts_reported():
     kaio.device_status()
+
+
+@pytest.mark.parametrize("m", [1, 16])
+def test_input_written_by_the_preceding_kernel(m, decode_split):
+    """A call must read x as left by the kernel just before it in the stream
+    (the decode kernel may start early under programmatic dependent launch and
+    must wait for its predecessor before reading): x is produced on the device
+    by a PyTorch kernel, in a chain of calls with no host synchronisation."""
+    import torch
+    n = k = 1024
+    inp = qkv_inputs(m, n, k, seed=31 + m)
+    x, wq, wk, wv, sq, sk, sv = qkv_to_dev(inp)
+    x_buf = torch.zeros_like(x)
+    outs = None
+    for step in range(3):
+        x_buf.copy_(x * (step + 1))        # a kernel writing x right before the call
+        outs = kaio.qkv_project_int4(x_buf, wq, wk, wv, sq, sk, sv)
+    torch.cuda.synchronize()
+    x3 = (inp.x.astype(np.float64) * 3).astype(np.float16)
+    refs = oracle.qkv_project_int4_ref(x3, inp.wq, inp.wk, inp.wv, inp.sq, inp.sk, inp.sv)
+    for o, r, name in zip(outs, refs, "QKV"):
+        assert_qkv_close(to_host(o), r, f"preceding-kernel x {name}")
+
+
+def test_chained_calls_read_the_previous_calls_output(decode_split):
+    """Call 2 takes call 1's Q output as its x (K = N) with no host
+    synchronisation between them: it must see all of call 1's output."""
+    import torch
+    m, n = 4, 512
+    inp = qkv_inputs(m, n, n, seed=77)
+    x, wq, wk, wv, sq, sk, sv = qkv_to_dev(inp)
+    q1, _, _ = kaio.qkv_project_int4(x, wq, wk, wv, sq, sk, sv)
+    q2, k2, v2 = kaio.qkv_project_int4(q1, wq, wk, wv, sq, sk, sv)
+    torch.cuda.synchronize()
+    q1_host = to_host(q1)
+    refs = oracle.qkv_project_int4_ref(q1_host, inp.wq, inp.wk, inp.wv, inp.sq, inp.sk, inp.sv)
+    for o, r, name in zip((q2, k2, v2), refs, "QKV"):
+        assert_qkv_close(to_host(o), r, f"chained {name}")
