@@ -31,6 +31,7 @@ DEFAULT_STEPS = {
     "qkv_batched_decode_m16_k8192_n8192": 40000,
     "qkv_prefill_m4096_k4096_n4096": 2000,
     "matmul_f16_m4096_n4096_k4096_fwd_bwd": 1000,
+    "matmul_f16out_m4096_n4096_k4096_fwd_bwd": 1000,
 }
 CONFIGS = {
     # name: (kind, M, N, K)
@@ -39,6 +40,8 @@ CONFIGS = {
     "qkv_batched_decode_m16_k8192_n8192": ("qkv", 16, 8192, 8192),
     "qkv_prefill_m4096_k4096_n4096": ("qkv", 4096, 4096, 4096),
     "matmul_f16_m4096_n4096_k4096_fwd_bwd": ("matmul", 4096, 4096, 4096),
+    # the same three GEMMs with the results rounded to f16 in the epilogue
+    "matmul_f16out_m4096_n4096_k4096_fwd_bwd": ("matmul16", 4096, 4096, 4096),
 }
 DEFAULT_CONFIG = "qkv_decode_m1_k4096_n4096"
 METRIC = "W4A16 QKV TFLOP/s and weight GB/s (1xGB300) as % of roofline"
@@ -251,20 +254,23 @@ def run_kaio(args, cfg_name, ws, rank, local, dist):
     else:
         a, b, g = dense_inputs(M, N, K, seed=0)
         A, B, G = dev(a), dev(b), dev(g)
-        C = torch.empty((M, N), dtype=torch.float32, device=device)
-        dA = torch.empty((M, K), dtype=torch.float32, device=device)
-        dB = torch.empty((K, N), dtype=torch.float32, device=device)
+        out_t = torch.float16 if kind == "matmul16" else torch.float32
+        C = torch.empty((M, N), dtype=out_t, device=device)
+        dA = torch.empty((M, K), dtype=out_t, device=device)
+        dB = torch.empty((K, N), dtype=out_t, device=device)
         lib = kaio.lib()
         sp = int(stream.cuda_stream)
+        fwd = lib.kaio_matmul_tc_f16 if kind == "matmul16" else lib.kaio_matmul_tc
+        bwd = lib.kaio_matmul_tc_backward_f16 if kind == "matmul16" else lib.kaio_matmul_tc_backward
 
         def step(i):
-            kaio.check(lib.kaio_matmul_tc(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K, sp))
-            kaio.check(lib.kaio_matmul_tc_backward(A.data_ptr(), B.data_ptr(), G.data_ptr(),
-                                                   dA.data_ptr(), dB.data_ptr(), M, N, K, sp))
+            kaio.check(fwd(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K, sp))
+            kaio.check(bwd(A.data_ptr(), B.data_ptr(), G.data_ptr(), dA.data_ptr(), dB.data_ptr(),
+                           M, N, K, sp))
 
         wbytes = 0
         units_bytes = 0
-        alg_bytes = 3 * (2 * M * K * 2 + M * N * 4)
+        alg_bytes = 3 * (2 * M * K * 2 + M * N * (2 if kind == "matmul16" else 4))
         flops = 3 * 2 * M * N * K
         kernel_file = "tc_kernels.cu"
         bound = "tensor"
@@ -363,7 +369,8 @@ def run_kaio(args, cfg_name, ws, rank, local, dist):
         value = ws * flops / per_step_s / 1e12
         unit = "TFLOP/s"
     line = {
-        "metric": METRIC if kind == "qkv" else "dense f16 tensor-core matmul fwd+bwd TFLOP/s",
+        "metric": METRIC if kind == "qkv" else ("dense f16 tensor-core matmul fwd+bwd TFLOP/s" if kind == "matmul"
+                                                else "dense f16 tensor-core matmul fwd+bwd, f16 results, TFLOP/s"),
         "value": round(value, 3),
         "unit": unit,
         "n_gpus": ws,
@@ -373,7 +380,8 @@ def run_kaio(args, cfg_name, ws, rank, local, dist):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "f16 (int4 weights, f32 accumulate)" if kind == "qkv" else "f16 (f32 accumulate)",
+        "dtype": "f16 (int4 weights, f32 accumulate)" if kind == "qkv" else
+                 ("f16 (f32 accumulate)" if kind == "matmul" else "f16 (f32 accumulate, f16 results)"),
         "data": "synthetic (seeded; weights rotate over sets totalling >= 3x L2)",
         "config": {"workload": cfg_name, "M": M, "N": N, "K": K, "parallelism": f"replicas x{ws}",
                    "l2": "inputs larger than L2 (weight sets rotated)" if kind == "qkv" else

@@ -145,6 +145,26 @@ int kaio_matmul_tc_backward(const void* a, const void* b, const void* g, float* 
                             uint32_t M, uint32_t N, uint32_t K, kaio_stream_t stream);
 
 /*
+ * kaio_matmul_tc with the result rounded to f16 in the kernel's epilogue
+ * (round-to-nearest-even of the f32 accumulator): c f16 [M, N]. The page's
+ * bridge casts matmul results to f16 afterwards ("kaio-candle 0.2.0 --
+ * src/matmul_tc_async.rs", MatmulTcAsyncOp::bwd, the casts of grad_a and
+ * grad_b to the input dtype); fusing the cast saves a pass over C.
+ * Arguments and errors: as kaio_matmul_tc, with c 16-byte aligned f16.
+ */
+int kaio_matmul_tc_f16(const void* a, const void* b, void* c, uint32_t M, uint32_t N, uint32_t K,
+                       kaio_stream_t stream);
+
+/*
+ * kaio_matmul_tc_backward with da f16 [M, K] and db f16 [K, N], each rounded
+ * from its f32 accumulator in the kernel (the page casts both to f16 after
+ * its matmuls, "kaio-candle 0.2.0 -- src/matmul_tc_async.rs",
+ * MatmulTcAsyncOp::bwd). Arguments and errors: as kaio_matmul_tc_backward.
+ */
+int kaio_matmul_tc_backward_f16(const void* a, const void* b, const void* g, void* da, void* db,
+                                uint32_t M, uint32_t N, uint32_t K, kaio_stream_t stream);
+
+/*
  * Dequantise packed INT4 weights to f16, exactly as the projection kernels do
  * before their multiply: out[k, n] = RN_f16(int4(W[k, n]) * s[k/128, n]).
  * A test entry for bit-exact comparison of the dequant stage.

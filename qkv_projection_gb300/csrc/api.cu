@@ -357,13 +357,14 @@ int kaio_qkv_project_int4_noalloc(const void* x, const uint32_t* wq, const uint3
   return KAIO_OK;
 }
 
-int kaio_matmul_tc(const void* a, const void* b, float* c, uint32_t M, uint32_t N, uint32_t K,
-                   kaio_stream_t stream_) {
-  g_last_error.clear();
-  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+namespace {
+
+// C = A @ B with the result stored as f32 (esize 4) or f16 (esize 2).
+int matmul_impl(const void* a, const void* b, void* c, size_t esize, uint32_t M, uint32_t N,
+                uint32_t K, cudaStream_t stream) {
   const size_t m = M, n = N, kk = K;
   const Span in[2] = {{"a", a, m * kk * 2}, {"b", b, kk * n * 2}};
-  const Span out[1] = {{"c", c, m * n * 4}};
+  const Span out[1] = {{"c", c, m * n * esize}};
   KAIO_TRY(check_not_null(in, 2));
   KAIO_TRY(check_not_null(out, 1));
   if (K % 8 != 0 || N % 8 != 0)
@@ -382,18 +383,17 @@ int kaio_matmul_tc(const void* a, const void* b, float* c, uint32_t M, uint32_t 
   KAIO_TRY(check_on_device(in, 2, dev));
   KAIO_TRY(check_on_device(out, 1, dev));
   cudaError_t e = kaio::launch_tc_gemm(a, b, c, {static_cast<int>(M), static_cast<int>(N), static_cast<int>(K)},
-                                       /*a_mn=*/false, /*b_mn=*/true, info.sms, stream);
+                                       /*a_mn=*/false, /*b_mn=*/true, esize == 2, info.sms, stream);
   if (e != cudaSuccess) return cuda_fail(e, "tcgen05 matmul launch");
   return KAIO_OK;
 }
 
-int kaio_matmul_tc_backward(const void* a, const void* b, const void* g, float* da, float* db,
-                            uint32_t M, uint32_t N, uint32_t K, kaio_stream_t stream_) {
-  g_last_error.clear();
-  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+// (dA, dB) = (G @ B^T, A^T @ G) stored as f32 (esize 4) or f16 (esize 2).
+int matmul_backward_impl(const void* a, const void* b, const void* g, void* da, void* db,
+                         size_t esize, uint32_t M, uint32_t N, uint32_t K, cudaStream_t stream) {
   const size_t m = M, n = N, kk = K;
   const Span in[3] = {{"a", a, m * kk * 2}, {"b", b, kk * n * 2}, {"g", g, m * n * 2}};
-  const Span out[2] = {{"da", da, m * kk * 4}, {"db", db, kk * n * 4}};
+  const Span out[2] = {{"da", da, m * kk * esize}, {"db", db, kk * n * esize}};
   KAIO_TRY(check_not_null(in, 3));
   KAIO_TRY(check_not_null(out, 2));
   if (K % 8 != 0 || N % 8 != 0)
@@ -412,17 +412,44 @@ int kaio_matmul_tc_backward(const void* a, const void* b, const void* g, float* 
   }
   KAIO_TRY(check_on_device(in, 3, dev));
   KAIO_TRY(check_on_device(out, 2, dev));
+  const bool f16 = esize == 2;
   // dA[M, K] = G[M, N] @ B^T: Aop = G stored [M][N] (K-major over N);
   //   Bop = B^T, an N x K operand whose storage B[K][N] is [No][Ko] (K-major).
   cudaError_t e = kaio::launch_tc_gemm(g, b, da, {static_cast<int>(M), static_cast<int>(K), static_cast<int>(N)},
-                                       false, false, info.sms, stream);
+                                       false, false, f16, info.sms, stream);
   if (e != cudaSuccess) return cuda_fail(e, "tcgen05 matmul launch (dA)");
   // dB[K, N] = A^T @ G: Aop = A^T, a K x M operand stored A[M][K] = [Ko][Mo]
   //   (MN-major); Bop = G, M x N stored [Ko][No] (MN-major).
   e = kaio::launch_tc_gemm(a, g, db, {static_cast<int>(K), static_cast<int>(N), static_cast<int>(M)},
-                           true, true, info.sms, stream);
+                           true, true, f16, info.sms, stream);
   if (e != cudaSuccess) return cuda_fail(e, "tcgen05 matmul launch (dB)");
   return KAIO_OK;
+}
+
+}  // namespace
+
+int kaio_matmul_tc(const void* a, const void* b, float* c, uint32_t M, uint32_t N, uint32_t K,
+                   kaio_stream_t stream) {
+  g_last_error.clear();
+  return matmul_impl(a, b, c, 4, M, N, K, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int kaio_matmul_tc_f16(const void* a, const void* b, void* c, uint32_t M, uint32_t N, uint32_t K,
+                       kaio_stream_t stream) {
+  g_last_error.clear();
+  return matmul_impl(a, b, c, 2, M, N, K, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int kaio_matmul_tc_backward(const void* a, const void* b, const void* g, float* da, float* db,
+                            uint32_t M, uint32_t N, uint32_t K, kaio_stream_t stream) {
+  g_last_error.clear();
+  return matmul_backward_impl(a, b, g, da, db, 4, M, N, K, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int kaio_matmul_tc_backward_f16(const void* a, const void* b, const void* g, void* da, void* db,
+                                uint32_t M, uint32_t N, uint32_t K, kaio_stream_t stream) {
+  g_last_error.clear();
+  return matmul_backward_impl(a, b, g, da, db, 2, M, N, K, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int kaio_dequant_int4_debug(const uint32_t* w, const void* s, void* out, uint32_t K, uint32_t N,

@@ -89,11 +89,12 @@ struct GemmShape {
   int M, N, K;              // C[M, N] = sum_k Aop[M, k] * Bop[k, N]
 };
 
-// Dense f16 x f16 -> f32. a_mn / b_mn select the operand storage:
+// Dense f16 x f16 -> f32 accumulate, stored as f32 or (c_f16) f16. a_mn / b_mn
+// select the operand storage:
 //   Aop K-major: A stored [M][K];  MN-major: A stored [K][M]
 //   Bop K-major: B stored [N][K];  MN-major: B stored [K][N]
-cudaError_t launch_tc_gemm(const void* a, const void* b, float* c, GemmShape sh, bool a_mn,
-                           bool b_mn, int num_sms, cudaStream_t stream);
+cudaError_t launch_tc_gemm(const void* a, const void* b, void* c, GemmShape sh, bool a_mn,
+                           bool b_mn, bool c_f16, int num_sms, cudaStream_t stream);
 
 // W4A16 fused projection for M >= 17 on tcgen05 (weights as the TMEM operand).
 cudaError_t launch_tc_w4a16(const __half* x, const uint32_t* const w[3], const __half* const s[3],

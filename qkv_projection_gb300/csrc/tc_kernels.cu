@@ -50,12 +50,14 @@ constexpr uint32_t GTMEM_COLS = 512;           // 2 x 256 f32 accumulators
 constexpr size_t GSMEM = static_cast<size_t>(GSTAGES) * GSTAGE_BYTES + 1024;
 
 struct GemmParams {
-  float* c;
+  void* c;              // f32 or f16 [M, N]
   int M, N, K;
   int m_blocks, tiles;
 };
 
-template <bool A_MN, bool B_MN>
+// C16: the epilogue rounds the f32 accumulators to f16 (round-to-nearest-even)
+// and stores f16, fusing the cast the page's backward applies afterwards.
+template <bool A_MN, bool B_MN, bool C16>
 __global__ void __launch_bounds__(GTHREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const GemmParams p) {
@@ -173,7 +175,6 @@ __global__ void __launch_bounds__(GTHREADS, 1)
       if (!mbar_wait(&acc_full[buf], aph, abort, &g_tc_err)) break;
       tc_fence_after();
       const int row = m0 + 32 * sp + lane;
-      float* crow = p.c + static_cast<size_t>(row) * p.N;
 #pragma unroll 1
       for (int ch = 0; ch < GBN / 32; ++ch) {
         uint32_t r[32];
@@ -184,10 +185,21 @@ __global__ void __launch_bounds__(GTHREADS, 1)
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
             const int col = col0 + 4 * q;
-            if (col < p.N)
+            if (col >= p.N) continue;
+            if (C16) {
+              __half* crow = static_cast<__half*>(p.c) + static_cast<size_t>(row) * p.N;
+              const __half2 lo = __floats2half2_rn(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]));
+              const __half2 hi = __floats2half2_rn(__uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
+              uint2 u;
+              u.x = *reinterpret_cast<const uint32_t*>(&lo);
+              u.y = *reinterpret_cast<const uint32_t*>(&hi);
+              *reinterpret_cast<uint2*>(crow + col) = u;
+            } else {
+              float* crow = static_cast<float*>(p.c) + static_cast<size_t>(row) * p.N;
               *reinterpret_cast<float4*>(crow + col) =
                   make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
                               __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
+            }
           }
         }
       }
@@ -527,8 +539,8 @@ static cudaError_t map_error(CUresult r) {
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-cudaError_t launch_tc_gemm(const void* a, const void* b, float* c, GemmShape sh, bool a_mn,
-                           bool b_mn, int num_sms, cudaStream_t stream) {
+cudaError_t launch_tc_gemm(const void* a, const void* b, void* c, GemmShape sh, bool a_mn,
+                           bool b_mn, bool c_f16, int num_sms, cudaStream_t stream) {
   CUtensorMap ta, tb;
   CUresult r;
   // Aop is [M x K]; stored [M][K] (K-major) or [K][M] (MN-major).
@@ -559,16 +571,22 @@ cudaError_t launch_tc_gemm(const void* a, const void* b, float* c, GemmShape sh,
   const int grid = std::min(p.tiles, num_sms);
 
   cudaError_t e;
-#define KAIO_LAUNCH_GEMM(AM, BM_)                                                               \
-  do {                                                                                          \
-    e = ensure_smem_limit(reinterpret_cast<const void*>(tc_gemm_kernel<AM, BM_>), (int)GSMEM); \
-    if (e != cudaSuccess) return e;                                                             \
-    tc_gemm_kernel<AM, BM_><<<grid, GTHREADS, GSMEM, stream>>>(ta, tb, p);                      \
+#define KAIO_LAUNCH_GEMM(AM, BM_, C16_)                                                             \
+  do {                                                                                              \
+    e = ensure_smem_limit(reinterpret_cast<const void*>(tc_gemm_kernel<AM, BM_, C16_>), (int)GSMEM); \
+    if (e != cudaSuccess) return e;                                                                 \
+    tc_gemm_kernel<AM, BM_, C16_><<<grid, GTHREADS, GSMEM, stream>>>(ta, tb, p);                    \
   } while (0)
-  if (!a_mn && b_mn) KAIO_LAUNCH_GEMM(false, true);
-  else if (!a_mn && !b_mn) KAIO_LAUNCH_GEMM(false, false);
-  else if (a_mn && b_mn) KAIO_LAUNCH_GEMM(true, true);
-  else KAIO_LAUNCH_GEMM(true, false);
+#define KAIO_LAUNCH_GEMM_C(AM, BM_)                  \
+  do {                                               \
+    if (c_f16) KAIO_LAUNCH_GEMM(AM, BM_, true);      \
+    else KAIO_LAUNCH_GEMM(AM, BM_, false);           \
+  } while (0)
+  if (!a_mn && b_mn) KAIO_LAUNCH_GEMM_C(false, true);
+  else if (!a_mn && !b_mn) KAIO_LAUNCH_GEMM_C(false, false);
+  else if (a_mn && b_mn) KAIO_LAUNCH_GEMM_C(true, true);
+  else KAIO_LAUNCH_GEMM_C(true, false);
+#undef KAIO_LAUNCH_GEMM_C
 #undef KAIO_LAUNCH_GEMM
   return cudaGetLastError();
 }

@@ -31,6 +31,8 @@ _SIGNATURES = {
     "kaio_qkv_project_int4_noalloc": ([_vp] * 10 + [_u32, _u32, _u32, _vp], _i32),
     "kaio_matmul_tc": ([_vp, _vp, _vp, _u32, _u32, _u32, _vp], _i32),
     "kaio_matmul_tc_backward": ([_vp] * 5 + [_u32, _u32, _u32, _vp], _i32),
+    "kaio_matmul_tc_f16": ([_vp, _vp, _vp, _u32, _u32, _u32, _vp], _i32),
+    "kaio_matmul_tc_backward_f16": ([_vp] * 5 + [_u32, _u32, _u32, _vp], _i32),
     "kaio_dequant_int4_debug": ([_vp, _vp, _vp, _u32, _u32, _i32, _vp], _i32),
     "kaio_qkv_path": ([_u32], _i32),
     "kaio_last_error": ([], ctypes.c_char_p),
@@ -150,8 +152,9 @@ def qkv_project_int4(x, w_q_packed, w_k_packed, w_v_packed, scales_q, scales_k, 
     return out
 
 
-def matmul_tc(a, b, out=None, stream=None):
-    """C = A @ B on the tensor cores: a f16 [M, K], b f16 [K, N] -> f32 [M, N]."""
+def matmul_tc(a, b, out=None, stream=None, out_dtype=None):
+    """C = A @ B on the tensor cores: a f16 [M, K], b f16 [K, N] -> [M, N] in
+    f32 (default) or f16 (rounded in the kernel's epilogue)."""
     torch = _torch()
     _need(a, "a", (torch.float16,))
     _need(b, "b", (torch.float16,))
@@ -159,15 +162,21 @@ def matmul_tc(a, b, out=None, stream=None):
     k2, n = b.shape
     if k != k2:
         raise ValueError(f"K mismatch between inputs: a is [{m}, {k}], b is [{k2}, {n}]")
+    if out_dtype is None:
+        out_dtype = out.dtype if out is not None else torch.float32
+    if out_dtype not in (torch.float32, torch.float16):
+        raise ValueError(f"out_dtype must be float32 or float16, got {out_dtype}")
     if out is None:
-        out = torch.empty((m, n), dtype=torch.float32, device=a.device)
-    _need(out, "c", (torch.float32,), (m, n))
-    check(lib().kaio_matmul_tc(a.data_ptr(), b.data_ptr(), out.data_ptr(), m, n, k, _stream_ptr(stream)))
+        out = torch.empty((m, n), dtype=out_dtype, device=a.device)
+    _need(out, "c", (out_dtype,), (m, n))
+    fn = lib().kaio_matmul_tc if out_dtype == torch.float32 else lib().kaio_matmul_tc_f16
+    check(fn(a.data_ptr(), b.data_ptr(), out.data_ptr(), m, n, k, _stream_ptr(stream)))
     return out
 
 
-def matmul_tc_backward(a, b, g, stream=None):
-    """(dA, dB) = (G @ B^T, A^T @ G) in f32 for C = A @ B, with g f16 [M, N]."""
+def matmul_tc_backward(a, b, g, stream=None, out_dtype=None):
+    """(dA, dB) = (G @ B^T, A^T @ G) for C = A @ B, with g f16 [M, N]; the
+    results are f32 (default) or f16 (rounded in the kernels' epilogues)."""
     torch = _torch()
     _need(a, "a", (torch.float16,))
     _need(b, "b", (torch.float16,))
@@ -175,10 +184,14 @@ def matmul_tc_backward(a, b, g, stream=None):
     n = b.shape[1]
     _need(b, "b", (torch.float16,), (k, n))
     _need(g, "g", (torch.float16,), (m, n))
-    da = torch.empty((m, k), dtype=torch.float32, device=a.device)
-    db = torch.empty((k, n), dtype=torch.float32, device=a.device)
-    check(lib().kaio_matmul_tc_backward(a.data_ptr(), b.data_ptr(), g.data_ptr(), da.data_ptr(),
-                                        db.data_ptr(), m, n, k, _stream_ptr(stream)))
+    out_dtype = torch.float32 if out_dtype is None else out_dtype
+    if out_dtype not in (torch.float32, torch.float16):
+        raise ValueError(f"out_dtype must be float32 or float16, got {out_dtype}")
+    da = torch.empty((m, k), dtype=out_dtype, device=a.device)
+    db = torch.empty((k, n), dtype=out_dtype, device=a.device)
+    fn = lib().kaio_matmul_tc_backward if out_dtype == torch.float32 else lib().kaio_matmul_tc_backward_f16
+    check(fn(a.data_ptr(), b.data_ptr(), g.data_ptr(), da.data_ptr(), db.data_ptr(), m, n, k,
+             _stream_ptr(stream)))
     return da, db
 
 

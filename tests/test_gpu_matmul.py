@@ -72,3 +72,42 @@ def test_forward_identity_exact():
 
 def test_no_device_timeouts_reported():
     kaio.device_status()
+
+
+@pytest.mark.parametrize("m,n,k", [(128, 256, 64), (1, 8, 8), (130, 264, 136), (257, 520, 1000),
+                                   (512, 512, 512)])
+def test_forward_f16_output(m, n, k):
+    """The f16-output variant stores RN_f16 of the same f32 accumulator the f32
+    variant stores (bit for bit), and stays within the matmul tolerance."""
+    import torch
+    a, b, _ = dense_inputs(m, n, k, seed=m + 2 * n + k)
+    ad, bd = to_dev(a), to_dev(b)
+    c32 = to_host(kaio.matmul_tc(ad, bd))
+    c16 = kaio.matmul_tc(ad, bd, out_dtype=torch.float16)
+    assert c16.dtype == torch.float16
+    c16 = to_host(c16)
+    assert np.array_equal(c16.view(np.uint16), c32.astype(np.float16).view(np.uint16))
+    assert rel_frobenius(c16.astype(np.float64), oracle.matmul_ref(a, b)) <= TOL
+
+
+@pytest.mark.parametrize("m,n,k", [(128, 256, 64), (136, 264, 200), (64, 8, 8)])
+def test_backward_f16_output(m, n, k):
+    import torch
+    a, b, g = dense_inputs(m, n, k, seed=5 * m + n)
+    ad, bd, gd = to_dev(a), to_dev(b), to_dev(g)
+    da32, db32 = (to_host(t) for t in kaio.matmul_tc_backward(ad, bd, gd))
+    da16, db16 = (to_host(t) for t in kaio.matmul_tc_backward(ad, bd, gd, out_dtype=torch.float16))
+    assert np.array_equal(da16.view(np.uint16), da32.astype(np.float16).view(np.uint16))
+    assert np.array_equal(db16.view(np.uint16), db32.astype(np.float16).view(np.uint16))
+    ra, rb = oracle.matmul_backward_ref(a, b, g)
+    assert rel_frobenius(da16.astype(np.float64), ra) <= TOL
+    assert rel_frobenius(db16.astype(np.float64), rb) <= TOL
+
+
+def test_f16_output_4096_sampled_rows():
+    import torch
+    a, b, _ = dense_inputs(4096, 4096, 4096, seed=0)
+    c = to_host(kaio.matmul_tc(to_dev(a), to_dev(b), out_dtype=torch.float16))
+    rows = np.unique(np.concatenate([np.random.default_rng(3).choice(4096, 48, replace=False),
+                                     [0, 127, 128, 4095]]))
+    assert rel_frobenius(c[rows].astype(np.float64), oracle.matmul_rows(a, b, rows)) <= TOL
