@@ -32,6 +32,8 @@ DEFAULT_STEPS = {
     "qkv_prefill_m4096_k4096_n4096": 2000,
     "matmul_f16_m4096_n4096_k4096_fwd_bwd": 1000,
     "matmul_f16out_m4096_n4096_k4096_fwd_bwd": 1000,
+    "dequant_bwd_bf16_outer8192_axis8192_g128": 4000,
+    "dequant_fwd_s8_f16_outer8192_axis8192_g128": 4000,
 }
 CONFIGS = {
     # name: (kind, M, N, K)
@@ -42,9 +44,27 @@ CONFIGS = {
     "matmul_f16_m4096_n4096_k4096_fwd_bwd": ("matmul", 4096, 4096, 4096),
     # the same three GEMMs with the results rounded to f16 in the epilogue
     "matmul_f16out_m4096_n4096_k4096_fwd_bwd": ("matmul16", 4096, 4096, 4096),
+    # per-group dequantisation: (kind, outer, axis, group)
+    "dequant_bwd_bf16_outer8192_axis8192_g128": ("dqbwd", 8192, 8192, 128),
+    "dequant_fwd_s8_f16_outer8192_axis8192_g128": ("dqfwd", 8192, 8192, 128),
 }
+# element types of the per-group dequantisation workloads: (float type, quantised type)
+DEQUANT_TYPES = {"dqbwd": ("bf16", "s8"), "dqfwd": ("f16", "s8")}
 DEFAULT_CONFIG = "qkv_decode_m1_k4096_n4096"
 METRIC = "W4A16 QKV TFLOP/s and weight GB/s (1xGB300) as % of roofline"
+METRICS = {
+    "qkv": METRIC,
+    "matmul": "dense f16 tensor-core matmul fwd+bwd TFLOP/s",
+    "matmul16": "dense f16 tensor-core matmul fwd+bwd, f16 results, TFLOP/s",
+    "dqbwd": "per-group dequantisation backward GB/s (dy + scale read, dx written)",
+    "dqfwd": "per-group dequantisation GB/s (q + scale read, out written)",
+}
+
+
+def config_shape(kind, a, b, c):
+    if kind in DEQUANT_TYPES:
+        return {"outer": a, "axis": b, "group": c}
+    return {"M": a, "N": b, "K": c}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_BYTES = 129 * 1024 * 1024
 
@@ -57,6 +77,15 @@ def qkv_bytes(m, n, k):
 
 def qkv_flops(m, n, k):
     return 3 * 2 * m * n * k
+
+
+def dequant_bytes(kind, outer, axis, group):
+    """Algorithmic bytes of one per-group dequantisation call: the input and
+    the scales read once, the output written once."""
+    fdt, _ = DEQUANT_TYPES[kind]
+    fsz = {"f32": 4, "f64": 8, "f16": 2, "bf16": 2}[fdt]
+    in_sz = fsz if kind == "dqbwd" else 1
+    return outer * axis * (in_sz + fsz) + outer * (axis // group) * fsz
 
 
 def load_peaks():
@@ -251,6 +280,42 @@ def run_kaio(args, cfg_name, ws, rank, local, dist):
             kernel_file = "tc_kernels.cu"
         bound = "hbm" if M <= 16 else "tensor"
         launches_per_step = 1
+    elif kind in DEQUANT_TYPES:
+        from qkv_projection_gb300.inputs import dequant_group_inputs
+        outer, axis, group = M, N, K
+        fdt, qdt = DEQUANT_TYPES[kind]
+        dy, q, sc = dequant_group_inputs(outer, axis, group, fdt, seed=0, q_dtype=qdt)
+        tdt = {"f32": torch.float32, "f64": torch.float64, "f16": torch.float16, "bf16": torch.bfloat16}[fdt]
+
+        def fdev(a):
+            return dev(a.view(np.int16)).view(tdt) if fdt == "bf16" else dev(a)
+        # Two input/output sets, alternated, so that every call streams from HBM
+        # (each set alone is at least L2-sized).
+        src = fdev(dy) if kind == "dqbwd" else dev(q)
+        S = fdev(sc)
+        srcs = [src, src.clone()]
+        outs = [torch.empty((outer, axis), dtype=tdt, device=device) for _ in range(2)]
+        lib = kaio.lib()
+        sp = int(stream.cuda_stream)
+        fcode = kaio._float_code(tdt)
+        qcode = kaio.KAIO_DTYPE_S8 if qdt == "s8" else kaio.KAIO_DTYPE_U8
+
+        def step(i):
+            a, o = srcs[i % 2], outs[i % 2]
+            if kind == "dqbwd":
+                kaio.check(lib.kaio_dequantize_per_group_backward(fcode, qcode, outer, axis, group, a.data_ptr(),
+                                                                  S.data_ptr(), o.data_ptr(), sp))
+            else:
+                kaio.check(lib.kaio_dequantize_per_group(qcode, fcode, outer, axis, group, a.data_ptr(),
+                                                         S.data_ptr(), o.data_ptr(), sp))
+
+        wbytes = 0
+        units_bytes = dequant_bytes(kind, outer, axis, group)
+        alg_bytes = units_bytes
+        flops = outer * axis
+        kernel_file = "dequant_group.cu"
+        bound = "hbm"
+        launches_per_step = 1
     else:
         a, b, g = dense_inputs(M, N, K, seed=0)
         A, B, G = dev(a), dev(b), dev(g)
@@ -365,12 +430,24 @@ def run_kaio(args, cfg_name, ws, rank, local, dist):
     if kind == "qkv":
         value = ws * wbytes / per_step_s / 1e9
         unit = "GB/s"
+    elif kind in DEQUANT_TYPES:
+        value = ws * units_bytes / per_step_s / 1e9
+        unit = "GB/s"
     else:
         value = ws * flops / per_step_s / 1e12
         unit = "TFLOP/s"
+    metric = METRICS[kind]
+    dtype = {"qkv": "f16 (int4 weights, f32 accumulate)", "matmul": "f16 (f32 accumulate)",
+             "matmul16": "f16 (f32 accumulate, f16 results)",
+             "dqbwd": "bf16 (products exact in f32, rounded once)",
+             "dqfwd": "int8 -> f16 (products exact in f32, rounded once)"}[kind]
+    l2 = {"qkv": "inputs larger than L2 (weight sets rotated)",
+          "dqbwd": "two input/output sets of 2x128 MiB alternated (inputs larger than L2)",
+          "dqfwd": "two input/output sets of 64+128 MiB alternated (inputs larger than L2)"}.get(
+              kind, "operands 32 MiB each; no flush (compute-bound)")
+    shape = config_shape(kind, M, N, K)
     line = {
-        "metric": METRIC if kind == "qkv" else ("dense f16 tensor-core matmul fwd+bwd TFLOP/s" if kind == "matmul"
-                                                else "dense f16 tensor-core matmul fwd+bwd, f16 results, TFLOP/s"),
+        "metric": metric,
         "value": round(value, 3),
         "unit": unit,
         "n_gpus": ws,
@@ -380,20 +457,18 @@ def run_kaio(args, cfg_name, ws, rank, local, dist):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "f16 (int4 weights, f32 accumulate)" if kind == "qkv" else
-                 ("f16 (f32 accumulate)" if kind == "matmul" else "f16 (f32 accumulate, f16 results)"),
-        "data": "synthetic (seeded; weights rotate over sets totalling >= 3x L2)",
-        "config": {"workload": cfg_name, "M": M, "N": N, "K": K, "parallelism": f"replicas x{ws}",
-                   "l2": "inputs larger than L2 (weight sets rotated)" if kind == "qkv" else
-                         "operands 32 MiB each; no flush (compute-bound)"},
-        "tflops": round(ws * flops / per_step_s / 1e12, 3),
+        "dtype": dtype,
+        "data": "synthetic (seeded; weights rotate over sets totalling >= 3x L2)" if kind == "qkv" else
+                "synthetic (seeded)",
+        "config": {"workload": cfg_name, **shape, "parallelism": f"replicas x{ws}", "l2": l2},
+        "tflops": round(ws * flops / per_step_s / 1e12, 3) if kind not in DEQUANT_TYPES else None,
         "weight_gbs": round(ws * wbytes / per_step_s / 1e9, 3) if kind == "qkv" else None,
         "roofline": roof,
         "e2e": e2e,
         "gpu_launches": steps * launches_per_step,
         "clocks": clk.summary(),
     }
-    if not args.no_cpu_baseline and ws == 1 and kind == "qkv":
+    if not args.no_cpu_baseline and ws == 1 and kind != "matmul" and kind != "matmul16":
         line["cpu_baseline"] = cpu_baseline(cfg_name, budget_s=args.cpu_budget)
     return line
 
@@ -407,6 +482,8 @@ def oracle_step_fn(cfg_name, frac):
     from qkv_projection_gb300.inputs import qkv_inputs
 
     kind, M, N, K = CONFIGS[cfg_name]
+    if kind in DEQUANT_TYPES:
+        return dequant_oracle_step_fn(cfg_name, frac)
     inp = qkv_inputs(M, N, K, seed=0)
     ncols = max(8, int(round(N * frac)) // 8 * 8)
     cols = np.arange(ncols)
@@ -419,9 +496,34 @@ def oracle_step_fn(cfg_name, frac):
     return step, wbytes, ncols
 
 
+def dequant_oracle_step_fn(cfg_name, frac):
+    """One oracle evaluation of a per-group dequantisation on a row sample
+    (fraction `frac` of the outer rows); returns (step, bytes, rows)."""
+    from oracle import dequant_group as dg
+    from qkv_projection_gb300.inputs import dequant_group_inputs
+
+    kind, outer, axis, group = CONFIGS[cfg_name]
+    fdt, qdt = DEQUANT_TYPES[kind]
+    rows = max(1, int(round(outer * frac)))
+    dy, q, sc = dequant_group_inputs(rows, axis, group, fdt, seed=0, q_dtype=qdt)
+    nbytes = dequant_bytes(kind, rows, axis, group)
+
+    def step():
+        if kind == "dqbwd":
+            dg.dequantize_per_group_backward_ref(dy, sc, group, fdt)
+        else:
+            dg.dequantize_per_group_ref(q, sc, group, fdt)
+    return step, nbytes, rows
+
+
 def cpu_baseline(cfg_name, budget_s=15.0):
     kind, M, N, K = CONFIGS[cfg_name]
-    step, wb, ncols = oracle_step_fn(cfg_name, 1.0 if N * K <= 4096 * 4096 else 0.125)
+    if kind in DEQUANT_TYPES:
+        step, wb, nrows = dequant_oracle_step_fn(cfg_name, 1.0 / 64)
+        what = f"{nrows} of {M} rows"
+    else:
+        step, wb, ncols = oracle_step_fn(cfg_name, 1.0 if N * K <= 4096 * 4096 else 0.125)
+        what = f"{ncols} of {N} columns"
     t0 = time.perf_counter()
     step()
     one = time.perf_counter() - t0
@@ -432,7 +534,7 @@ def cpu_baseline(cfg_name, budget_s=15.0):
     dt = time.perf_counter() - t0
     return {"value": round(wb * reps / dt / 1e9, 4), "unit": "GB/s", "cores": os.cpu_count(),
             "kind": "oracle",
-            "sample": f"{reps} oracle evaluations of {cfg_name} on {ncols} of {N} columns "
+            "sample": f"{reps} oracle evaluations of {cfg_name} on {what} "
                       f"(numpy float64; BLAS may use up to {os.cpu_count()} threads)"}
 
 
@@ -440,15 +542,18 @@ def run_reference(args, cfg_name, ws, rank):
     kind, M, N, K = CONFIGS[cfg_name]
     if rank != 0:
         return None
-    if kind != "qkv":
-        return {"impl": "reference", "unavailable": "oracle arm covers the W4A16 workloads only"}
-    # Size each step's sample so the whole run takes about --ref-seconds.
+    if kind in ("matmul", "matmul16"):
+        return {"impl": "reference", "unavailable": "the oracle arm covers the W4A16 and dequantisation workloads"}
+    # Size each step's sample (columns of W, or rows of a dequantisation) so the
+    # whole run takes about --ref-seconds.
+    dq = kind in DEQUANT_TYPES
+    extent = M if dq else N
     total_steps = args.steps + max(args.warmup, 3)
-    probe, _, _ = oracle_step_fn(cfg_name, 1.0 / 64)
+    probe, _, n_probe = oracle_step_fn(cfg_name, 1.0 / 64)
     t0 = time.perf_counter()
     probe()
-    per_col = (time.perf_counter() - t0) / max(8, N // 64)
-    frac = min(1.0, max(8.0 / N, args.ref_seconds / total_steps / max(per_col, 1e-9) / N))
+    per_unit = (time.perf_counter() - t0) / n_probe
+    frac = min(1.0, max(8.0 / extent, args.ref_seconds / total_steps / max(per_unit, 1e-9) / extent))
     step, wb, ncols = oracle_step_fn(cfg_name, frac)
     for _ in range(max(args.warmup, 3)):
         step()
@@ -457,14 +562,14 @@ def run_reference(args, cfg_name, ws, rank):
         step()
     dt = time.perf_counter() - t0
     value = wb * args.steps / dt / 1e9
-    sample = (f"each step: one oracle evaluation of {cfg_name} on {ncols} of {N} columns "
-              f"(numpy float64)")
+    sample = (f"each step: one oracle evaluation of {cfg_name} on {ncols} of {extent} "
+              f"{'rows' if dq else 'columns'} (numpy float64)")
     return {
-        "impl": "reference", "metric": METRIC, "value": round(value, 5), "unit": "GB/s",
+        "impl": "reference", "metric": METRICS[kind], "value": round(value, 5), "unit": "GB/s",
         "n_gpus": ws, "steps": args.steps, "warmup": max(args.warmup, 3),
         "ms_per_step": round(dt / args.steps * 1e3, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
-        "config": {"workload": cfg_name, "M": M, "N": N, "K": K},
+        "config": {"workload": cfg_name, **config_shape(kind, M, N, K)},
         "cpu_baseline": {"value": round(value, 5), "unit": "GB/s", "cores": os.cpu_count(),
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 5), "unit": "GB/s", "h2d_bytes_per_step": 0,

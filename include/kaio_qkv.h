@@ -164,6 +164,51 @@ int kaio_matmul_tc_f16(const void* a, const void* b, void* c, uint32_t M, uint32
 int kaio_matmul_tc_backward_f16(const void* a, const void* b, const void* g, void* da, void* db,
                                 uint32_t M, uint32_t N, uint32_t K, kaio_stream_t stream);
 
+/* Element types of the per-group dequantisation entry points. bf16 values are
+ * passed as their 16-bit patterns. */
+typedef enum {
+  KAIO_DTYPE_F32 = 0,
+  KAIO_DTYPE_F64 = 1,
+  KAIO_DTYPE_F16 = 2,
+  KAIO_DTYPE_BF16 = 3,
+  KAIO_DTYPE_S8 = 4,
+  KAIO_DTYPE_U8 = 5
+} kaio_dtype;
+
+/*
+ * Straight-through backward of the per-group dequantisation
+ * ("baracuda-kernels -- src/quantize/dequantize_per_group_backward.rs",
+ * module doc and DequantizePerGroupBackwardPlan):
+ *
+ *   dx[i, j] = dy[i, j] * scale[i, j / group]
+ *
+ *   dy, dx  dtype [outer, axis], row-major        dtype: F32, F64, F16 or BF16
+ *   scale   dtype [outer, axis / group]            (groups along the last axis)
+ *   q_dtype the forward's quantised type, S8 or U8 (checked, as the page's
+ *           plan does; it does not change the result)
+ * Each product is rounded once to dtype (deterministic, bit-stable). dx may be
+ * dy itself (in place); no other overlap is allowed. All pointers are device
+ * memory of the current device owned by the caller, aligned to their element
+ * size. Asynchronous on `stream`.
+ * Errors: KAIO_ERR_INVALID_VALUE for an unsupported dtype or q_dtype, negative
+ * outer or axis, group <= 0, axis not a multiple of group, a null pointer,
+ * overlap, memory not on the current device; KAIO_ERR_MISALIGNED; an empty
+ * problem (outer * axis == 0) returns KAIO_OK without launching.
+ */
+int kaio_dequantize_per_group_backward(int dtype, int q_dtype, int32_t outer, int32_t axis, int32_t group,
+                                       const void* dy, const void* scale, void* dx, kaio_stream_t stream);
+
+/*
+ * The per-group dequantisation itself: out[i, j] = dtype(q[i, j]) *
+ * scale[i, j / group], q int8 (S8) or uint8 (U8) [outer, axis], no zero point.
+ * The page names this plan (DequantizePerGroupPlan, whose backward is above)
+ * but does not show it; this is the plainest reading of its backward's
+ * straight-through definition. Arguments, layout, rounding and errors as the
+ * backward, with q in place of dy (no overlap with out allowed).
+ */
+int kaio_dequantize_per_group(int q_dtype, int dtype, int32_t outer, int32_t axis, int32_t group,
+                              const void* q, const void* scale, void* out, kaio_stream_t stream);
+
 /*
  * Dequantise packed INT4 weights to f16, exactly as the projection kernels do
  * before their multiply: out[k, n] = RN_f16(int4(W[k, n]) * s[k/128, n]).

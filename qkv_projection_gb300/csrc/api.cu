@@ -452,6 +452,82 @@ int kaio_matmul_tc_backward_f16(const void* a, const void* b, const void* g, voi
   return matmul_backward_impl(a, b, g, da, db, 2, M, N, K, reinterpret_cast<cudaStream_t>(stream));
 }
 
+namespace {
+
+bool float_type(int dtype, kaio::FloatType* t, size_t* esize) {
+  switch (dtype) {
+    case KAIO_DTYPE_F32: *t = kaio::FloatType::F32; *esize = 4; return true;
+    case KAIO_DTYPE_F64: *t = kaio::FloatType::F64; *esize = 8; return true;
+    case KAIO_DTYPE_F16: *t = kaio::FloatType::F16; *esize = 2; return true;
+    case KAIO_DTYPE_BF16: *t = kaio::FloatType::BF16; *esize = 2; return true;
+    default: return false;
+  }
+}
+
+// Shared by the per-group dequantisation and its backward, in the order the
+// page's plan checks them: element types, sizes and group, empty problem (Ok,
+// no launch), then pointers (null, alignment to the element size, overlap,
+// residency) and the device.
+int dequant_group_impl(bool backward, int dtype, int q_dtype, int32_t outer, int32_t axis, int32_t group,
+                       const void* in, const void* scale, void* out, cudaStream_t stream) {
+  kaio::FloatType t;
+  size_t es;
+  if (!float_type(dtype, &t, &es))
+    return fail(KAIO_ERR_INVALID_VALUE, "unsupported float type %d (f32, f64, f16 or bf16)", dtype);
+  if (q_dtype != KAIO_DTYPE_S8 && q_dtype != KAIO_DTYPE_U8)
+    return fail(KAIO_ERR_INVALID_VALUE, "the quantised type must be S8 or U8 (got %d)", q_dtype);
+  if (outer < 0 || axis < 0)
+    return fail(KAIO_ERR_INVALID_VALUE, "outer (%d) and axis (%d) must be non-negative", outer, axis);
+  if (group <= 0) return fail(KAIO_ERR_INVALID_VALUE, "group (%d) must be > 0", group);
+  if (axis % group != 0)
+    return fail(KAIO_ERR_INVALID_VALUE, "axis (%d) must be a multiple of group (%d)", axis, group);
+  const size_t total = static_cast<size_t>(outer) * static_cast<size_t>(axis);
+  if (total == 0) return KAIO_OK;
+  const size_t in_es = backward ? es : 1;
+  const char* in_name = backward ? "dy" : "q";
+  const char* out_name = backward ? "dx" : "out";
+  const Span sin{in_name, in, total * in_es};
+  const Span ssc{"scale", scale, static_cast<size_t>(outer) * (static_cast<size_t>(axis) / group) * es};
+  const Span sout{out_name, out, total * es};
+  const Span all[3] = {sin, ssc, sout};
+  KAIO_TRY(check_not_null(all, 3));
+  const size_t align[3] = {in_es, es, es};
+  for (int i = 0; i < 3; ++i)
+    if (reinterpret_cast<uintptr_t>(all[i].p) % align[i] != 0)
+      return fail(KAIO_ERR_MISALIGNED, "%s (%p) is not aligned to its %zu-byte elements", all[i].name,
+                  all[i].p, align[i]);
+  if (overlaps(sout, ssc)) return fail(KAIO_ERR_INVALID_VALUE, "%s overlaps scale", out_name);
+  // The backward may run in place (dx == dy); any other overlap is an error.
+  if (overlaps(sout, sin) && !(backward && in == out))
+    return fail(KAIO_ERR_INVALID_VALUE, "%s overlaps %s (only dx == dy exactly is allowed)", out_name, in_name);
+  int dev;
+  DeviceInfo info;
+  KAIO_TRY(current_device(&dev, &info));
+  KAIO_TRY(check_on_device(all, 3, dev));
+  const cudaError_t e =
+      backward ? kaio::launch_dequant_group_backward(t, in, scale, out, outer, axis, group, info.sms, stream)
+               : kaio::launch_dequant_group_forward(t, q_dtype == KAIO_DTYPE_U8, in, scale, out, outer, axis,
+                                                    group, info.sms, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "per-group dequantisation launch");
+  return KAIO_OK;
+}
+
+}  // namespace
+
+int kaio_dequantize_per_group_backward(int dtype, int q_dtype, int32_t outer, int32_t axis, int32_t group,
+                                       const void* dy, const void* scale, void* dx, kaio_stream_t stream) {
+  g_last_error.clear();
+  return dequant_group_impl(true, dtype, q_dtype, outer, axis, group, dy, scale, dx,
+                            reinterpret_cast<cudaStream_t>(stream));
+}
+
+int kaio_dequantize_per_group(int q_dtype, int dtype, int32_t outer, int32_t axis, int32_t group,
+                              const void* q, const void* scale, void* out, kaio_stream_t stream) {
+  g_last_error.clear();
+  return dequant_group_impl(false, dtype, q_dtype, outer, axis, group, q, scale, out,
+                            reinterpret_cast<cudaStream_t>(stream));
+}
+
 int kaio_dequant_int4_debug(const uint32_t* w, const void* s, void* out, uint32_t K, uint32_t N,
                             int variant, kaio_stream_t stream_) {
   g_last_error.clear();

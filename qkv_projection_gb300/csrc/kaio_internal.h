@@ -84,6 +84,16 @@ cudaError_t launch_tc_decode(const __half* x, const uint32_t* const w[3], const 
                              cudaStream_t stream);
 unsigned read_and_clear_tc_decode_errors();
 
+// ------------------------------------------------- per-group dequantisation
+enum class FloatType { F32, F64, F16, BF16 };
+// dx[i, j] = dy[i, j] * scale[i, j / group] over [outer, axis], in type t.
+cudaError_t launch_dequant_group_backward(FloatType t, const void* dy, const void* scale, void* dx,
+                                          int outer, int axis, int group, int num_sms, cudaStream_t stream);
+// out[i, j] = t(q[i, j]) * scale[i, j / group], q int8 (or uint8 if q_unsigned).
+cudaError_t launch_dequant_group_forward(FloatType t, bool q_unsigned, const void* q, const void* scale,
+                                         void* out, int outer, int axis, int group, int num_sms,
+                                         cudaStream_t stream);
+
 // ------------------------------------------------- tensor-core (tcgen05) paths
 struct GemmShape {
   int M, N, K;              // C[M, N] = sum_k Aop[M, k] * Bop[k, N]

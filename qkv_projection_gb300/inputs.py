@@ -80,3 +80,26 @@ def dense_inputs(m: int, n: int, k: int, seed: int = 0):
     b = rng.uniform(-1.0, 1.0, size=(k, n)).astype(np.float16)
     g = rng.standard_normal((m, n), dtype=np.float32).astype(np.float16)
     return a, b, g
+
+
+def dequant_group_inputs(outer: int, axis: int, group: int, dtype: str, seed: int = 0, q_dtype: str = "s8"):
+    """Seeded inputs of the per-group dequantisation and its backward.
+
+    Returns (dy, q, scale) as numpy arrays: dy [outer, axis] and scale
+    [outer, axis // group] in ``dtype`` (bf16 as uint16 bit patterns: the upper
+    half of a float32 draw), dy ~ N(0, 1), scale uniform in [0.005, 0.02];
+    q [outer, axis] uniform over all int8 (or uint8) values.
+    """
+    rng = np.random.default_rng(seed)
+    dy = rng.standard_normal((outer, axis))
+    sc = rng.uniform(0.005, 0.02, size=(outer, axis // group))
+    qd = np.int8 if q_dtype == "s8" else np.uint8
+    info = np.iinfo(qd)
+    q = rng.integers(info.min, info.max + 1, size=(outer, axis), dtype=np.int64).astype(qd)
+
+    def cast(a):
+        if dtype == "bf16":
+            return (a.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+        return a.astype({"f32": np.float32, "f64": np.float64, "f16": np.float16}[dtype])
+
+    return cast(dy), q, cast(sc)

@@ -23,6 +23,8 @@ KAIO_ERR_UNSUPPORTED_DEVICE = 3
 KAIO_ERR_CUDA = 4
 KAIO_ERR_DEVICE_TIMEOUT = 5
 
+KAIO_DTYPE_F32, KAIO_DTYPE_F64, KAIO_DTYPE_F16, KAIO_DTYPE_BF16, KAIO_DTYPE_S8, KAIO_DTYPE_U8 = range(6)
+
 _lib = None
 
 _vp, _u32, _i32 = ctypes.c_void_p, ctypes.c_uint32, ctypes.c_int
@@ -34,6 +36,8 @@ _SIGNATURES = {
     "kaio_matmul_tc_f16": ([_vp, _vp, _vp, _u32, _u32, _u32, _vp], _i32),
     "kaio_matmul_tc_backward_f16": ([_vp] * 5 + [_u32, _u32, _u32, _vp], _i32),
     "kaio_dequant_int4_debug": ([_vp, _vp, _vp, _u32, _u32, _i32, _vp], _i32),
+    "kaio_dequantize_per_group_backward": ([_i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp], _i32),
+    "kaio_dequantize_per_group": ([_i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp], _i32),
     "kaio_qkv_path": ([_u32], _i32),
     "kaio_last_error": ([], ctypes.c_char_p),
     "kaio_device_status": ([], _i32),
@@ -215,3 +219,55 @@ def qkv_path(m: int) -> int:
 def device_status() -> None:
     """Synchronise and raise if a kernel reported a bounded-wait timeout."""
     check(lib().kaio_device_status())
+
+
+def _float_code(dtype):
+    torch = _torch()
+    codes = {torch.float32: KAIO_DTYPE_F32, torch.float64: KAIO_DTYPE_F64,
+             torch.float16: KAIO_DTYPE_F16, torch.bfloat16: KAIO_DTYPE_BF16}
+    if dtype not in codes:
+        raise TypeError(f"dtype {dtype} is not one of float32, float64, float16, bfloat16")
+    return codes[dtype]
+
+
+def dequantize_per_group_backward(dy, scale, group: int, q_dtype=None, out=None, stream=None):
+    """dx[i, j] = dy[i, j] * scale[i, j // group] (straight-through backward of
+    the per-group dequantisation), for dy [outer, axis] and scale
+    [outer, axis // group] of one float type. q_dtype (int8 or uint8, default
+    int8) is the forward's quantised type; out may be dy itself (in place)."""
+    torch = _torch()
+    fdt = (torch.float32, torch.float64, torch.float16, torch.bfloat16)
+    _need(dy, "dy", fdt)
+    outer, axis = dy.shape
+    if group <= 0 or axis % group != 0:
+        raise ValueError(f"group ({group}) must be > 0 and divide axis ({axis})")
+    _need(scale, "scale", (dy.dtype,), (outer, axis // group))
+    q_dtype = torch.int8 if q_dtype is None else q_dtype
+    qcode = {torch.int8: KAIO_DTYPE_S8, torch.uint8: KAIO_DTYPE_U8}.get(q_dtype)
+    if qcode is None:
+        raise TypeError("q_dtype must be torch.int8 or torch.uint8")
+    if out is None:
+        out = torch.empty_like(dy)
+    _need(out, "dx", (dy.dtype,), (outer, axis))
+    check(lib().kaio_dequantize_per_group_backward(_float_code(dy.dtype), qcode, outer, axis, group,
+                                                   dy.data_ptr(), scale.data_ptr(), out.data_ptr(),
+                                                   _stream_ptr(stream)))
+    return out
+
+
+def dequantize_per_group(q, scale, group: int, out=None, stream=None):
+    """out[i, j] = T(q[i, j]) * scale[i, j // group] for q int8 or uint8
+    [outer, axis] and scale [outer, axis // group] of float type T."""
+    torch = _torch()
+    _need(q, "q", (torch.int8, torch.uint8))
+    outer, axis = q.shape
+    if group <= 0 or axis % group != 0:
+        raise ValueError(f"group ({group}) must be > 0 and divide axis ({axis})")
+    _need(scale, "scale", (torch.float32, torch.float64, torch.float16, torch.bfloat16), (outer, axis // group))
+    if out is None:
+        out = torch.empty((outer, axis), dtype=scale.dtype, device=q.device)
+    _need(out, "out", (scale.dtype,), (outer, axis))
+    qcode = KAIO_DTYPE_S8 if q.dtype == torch.int8 else KAIO_DTYPE_U8
+    check(lib().kaio_dequantize_per_group(qcode, _float_code(scale.dtype), outer, axis, group,
+                                          q.data_ptr(), scale.data_ptr(), out.data_ptr(), _stream_ptr(stream)))
+    return out

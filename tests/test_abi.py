@@ -146,3 +146,29 @@ def test_noalloc_entry_validation(L):
     q = list(p)
     q[4] += 2
     assert L.kaio_qkv_project_int4_noalloc(*q, 16, 128, 256, None) == MISALIGNED
+
+
+def test_dequant_group_validation_order(L):
+    """Checks in the page's order: element types, sizes and group, the empty
+    problem (Ok with null pointers), then pointers."""
+    F16, F32, F64, BF16, S8, U8 = (kaio.KAIO_DTYPE_F16, kaio.KAIO_DTYPE_F32, kaio.KAIO_DTYPE_F64,
+                                   kaio.KAIO_DTYPE_BF16, kaio.KAIO_DTYPE_S8, kaio.KAIO_DTYPE_U8)
+    bwd, fwd = L.kaio_dequantize_per_group_backward, L.kaio_dequantize_per_group
+    dy, sc, dx = 0x10000000, 0x20000000, 0x30000000
+    assert bwd(S8, S8, 2, 8, 4, dy, sc, dx, None) == INVALID and "float type" in kaio.last_error()
+    assert bwd(F16, F32, 2, 8, 4, dy, sc, dx, None) == INVALID and "S8 or U8" in kaio.last_error()
+    assert bwd(F16, S8, -1, 8, 4, dy, sc, dx, None) == INVALID and "non-negative" in kaio.last_error()
+    assert bwd(F16, S8, 2, 8, 0, dy, sc, dx, None) == INVALID and "> 0" in kaio.last_error()
+    assert bwd(F16, S8, 2, 10, 4, dy, sc, dx, None) == INVALID and "multiple of group" in kaio.last_error()
+    assert bwd(F16, S8, 0, 8, 4, None, None, None, None) == kaio.KAIO_OK
+    assert fwd(U8, BF16, 3, 0, 4, None, None, None, None) == kaio.KAIO_OK
+    assert bwd(F16, S8, 2, 8, 4, None, sc, dx, None) == INVALID and "null" in kaio.last_error()
+    assert bwd(F32, S8, 2, 8, 4, dy + 2, sc, dx, None) == MISALIGNED
+    assert bwd(F64, S8, 2, 8, 4, dy, sc + 4, dx, None) == MISALIGNED
+    assert fwd(S8, F16, 2, 8, 4, dy + 1, sc, dx, None) != MISALIGNED      # int8 input: any address
+    assert bwd(F16, S8, 2, 8, 4, dy, sc, sc + 2, None) == INVALID and "overlaps scale" in kaio.last_error()
+    assert bwd(F16, S8, 2, 8, 4, dy, sc, dy + 2, None) == INVALID and "overlaps" in kaio.last_error()
+    assert fwd(S8, F16, 2, 8, 4, dy, sc, dy, None) == INVALID and "overlaps" in kaio.last_error()
+    # exactly in place passes the argument checks; without a GPU it then fails on CUDA
+    st = bwd(F16, S8, 2, 8, 4, dy, sc, dy, None)
+    assert st != INVALID or "overlap" not in kaio.last_error()
