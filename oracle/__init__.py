@@ -1,4 +1,4 @@
-"""CPU oracle for the W4A16 fused QKV projection and the dense f16 matmul.
+"""CPU oracle for the W4A16 and W8A16 fused QKV projections and the dense f16 matmul.
 
 TEST INFRASTRUCTURE ONLY. Nothing in the product path imports this package:
 only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
@@ -20,4 +20,11 @@ from .w4a16 import (  # noqa: F401
     matmul_rows,
     matmul_backward_ref,
     ulp_f16,
+)
+from .w8a16 import (  # noqa: F401
+    unpack_int8,
+    pack_int8,
+    dequant_int8,
+    qkv_project_int8_ref,
+    qkv_project_int8_rows,
 )

@@ -1,4 +1,5 @@
-"""Seeded synthetic inputs for the W4A16 QKV projection and the dense f16 matmul.
+"""Seeded synthetic inputs for the W4A16 / W8A16 QKV projections, the dense f16
+matmul and the per-group dequantisation.
 
 This module only draws random numbers. It holds none of the method's
 arithmetic: packed weights are drawn as uniformly random 32-bit words, which is
@@ -11,6 +12,9 @@ Distributions (workload shapes of the W4A16 projection and the dense matmul):
 - ``x``: f16, standard normal, rounded to f16 by the dtype cast.
 - ``wq``/``wk``/``wv``: uint32 ``[K/8, N]``, uniform over all 2**32 words.
 - ``sq``/``sk``/``sv``: f16 ``[K/128, N]``, uniform in [0.005, 0.02].
+- W8A16 (``qkv_int8_inputs``): ``x`` as above; packed ``u32[K/4, N]`` words
+  uniform over all 2**32 words (every int8 byte equally likely); the three
+  per-projection f32 scales uniform in [5e-4, 2e-3].
 - dense ``a``/``b``: f16, uniform in [-1, 1]; backward ``g``: f16 standard normal.
 
 One ``numpy.random.Generator`` (PCG64) per call, seeded by ``seed``; tensors
@@ -71,6 +75,45 @@ def weight_sets(n: int, k: int, count: int, seed: int = 1):
              for _ in range(3)]
         out.append((*w, *s))
     return out
+
+
+@dataclass
+class QKV8Inputs:
+    x: np.ndarray   # f16 [M, K]
+    wq: np.ndarray  # u32 [K/4, N]
+    wk: np.ndarray
+    wv: np.ndarray
+    sq: float       # f32 scale of each projection
+    sk: float
+    sv: float
+
+    def weights(self):
+        return (self.wq, self.wk, self.wv)
+
+    def scales(self):
+        return (self.sq, self.sk, self.sv)
+
+    def args(self):
+        return (self.x, self.wq, self.wk, self.wv, self.sq, self.sk, self.sv)
+
+
+def qkv_int8_inputs(m: int, n: int, k: int, seed: int = 0) -> QKV8Inputs:
+    """Draw one W8A16 problem of shape (M, N, K); x, wq, wk, wv, sq, sk, sv in order."""
+    if k % 4:
+        raise ValueError(f"K={k} is not a multiple of 4")
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((m, k), dtype=np.float32).astype(np.float16)
+    w = [rng.integers(0, 2**32, size=(k // 4, n), dtype=np.uint32) for _ in range(3)]
+    s = [float(np.float32(rng.uniform(5e-4, 2e-3))) for _ in range(3)]
+    return QKV8Inputs(x, w[0], w[1], w[2], s[0], s[1], s[2])
+
+
+def weight_sets_int8(n: int, k: int, count: int, seed: int = 1):
+    """``count`` distinct packed (wq, wk, wv) INT8 weight sets (rotated between
+    timed launches so that every launch streams its weights from HBM)."""
+    rng = np.random.default_rng(seed)
+    return [tuple(rng.integers(0, 2**32, size=(k // 4, n), dtype=np.uint32) for _ in range(3))
+            for _ in range(count)]
 
 
 def dense_inputs(m: int, n: int, k: int, seed: int = 0):
