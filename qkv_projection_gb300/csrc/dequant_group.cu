@@ -180,8 +180,11 @@ cudaError_t launch_typed(const void* in_, const void* scale_, void* out_, int ou
   const int ngroups = axis / group;
   const bool aligned = reinterpret_cast<uintptr_t>(out) % 16 == 0 &&
                        reinterpret_cast<uintptr_t>(in) % Vec<T, A>::kInBytes == 0;
-  // Enough CTAs to keep every SM's memory pipes busy; the loops stride the rest.
-  const int max_blocks = num_sms * 8;
+  // One pass per thread (kUnroll vectors) where the grid allows: short-lived
+  // CTAs that the block scheduler refills measured faster on these streams
+  // than a persistent grid-stride grid (a ragged last wave of resident CTAs
+  // leaves HBM idle). Very large problems stride over the capped grid.
+  const int max_blocks = num_sms * 64;
   if (aligned && axis % kN == 0) {
     const long long nvec = total / kN;
     const long long want = (nvec + kThreads * kUnroll - 1) / (kThreads * kUnroll);

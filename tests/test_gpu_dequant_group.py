@@ -113,13 +113,24 @@ def test_empty_problems_are_no_ops():
 
 
 def test_backward_large_sampled_rows():
-    # a launch with many CTAs and the grid-stride loops wrapping several times
-    outer, axis, group = 2048, 4096, 128
+    # 10.5 M vectors of 8 elements: more than the capped grid (64 CTAs of 256
+    # threads x 4 vectors per SM on 152 SMs), so the grid-stride loop wraps
+    outer, axis, group = 8192, 10240, 128
     dy, _, sc = dequant_group_inputs(outer, axis, group, "bf16", seed=21)
     got = bits(kaio.dequantize_per_group_backward(to_dev(dy, "bf16"), to_dev(sc, "bf16"), group), "bf16")
     rows = np.unique(np.concatenate([np.random.default_rng(5).choice(outer, 64, replace=False), [0, outer - 1]]))
     ref = dg.dequantize_per_group_backward_ref(dy[rows], sc[rows], group, "bf16")
     assert np.array_equal(got[rows], ref_bits(ref, "bf16"))
+
+
+def test_forward_large_sampled_rows():
+    import torch
+    outer, axis, group = 8192, 10240, 64
+    _, q, sc = dequant_group_inputs(outer, axis, group, "f16", seed=22, q_dtype="u8")
+    got = bits(kaio.dequantize_per_group(torch.from_numpy(q).cuda(), to_dev(sc, "f16"), group), "f16")
+    rows = np.unique(np.concatenate([np.random.default_rng(6).choice(outer, 64, replace=False), [0, outer - 1]]))
+    ref = dg.dequantize_per_group_ref(q[rows], sc[rows], group, "f16")
+    assert np.array_equal(got[rows], ref_bits(ref, "f16"))
 
 
 def test_no_device_timeouts_or_errors():
