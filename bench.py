@@ -32,6 +32,9 @@ DEFAULT_STEPS = {
     "qkv_prefill_m4096_k4096_n4096": 2000,
     "matmul_f16_m4096_n4096_k4096_fwd_bwd": 1000,
     "matmul_f16out_m4096_n4096_k4096_fwd_bwd": 1000,
+    "qkv8_decode_m1_k4096_n4096": 50000,
+    "qkv8_batched_decode_m16_k8192_n8192": 20000,
+    "qkv8_prefill_m4096_k4096_n4096": 2000,
     "dequant_bwd_bf16_outer8192_axis8192_g128": 4000,
     "dequant_fwd_s8_f16_outer8192_axis8192_g128": 4000,
 }
@@ -44,6 +47,10 @@ CONFIGS = {
     "matmul_f16_m4096_n4096_k4096_fwd_bwd": ("matmul", 4096, 4096, 4096),
     # the same three GEMMs with the results rounded to f16 in the epilogue
     "matmul_f16out_m4096_n4096_k4096_fwd_bwd": ("matmul16", 4096, 4096, 4096),
+    # W8A16 (INT8 weights, one f32 scale per projection)
+    "qkv8_decode_m1_k4096_n4096": ("qkv8", 1, 4096, 4096),
+    "qkv8_batched_decode_m16_k8192_n8192": ("qkv8", 16, 8192, 8192),
+    "qkv8_prefill_m4096_k4096_n4096": ("qkv8", 4096, 4096, 4096),
     # per-group dequantisation: (kind, outer, axis, group)
     "dequant_bwd_bf16_outer8192_axis8192_g128": ("dqbwd", 8192, 8192, 128),
     "dequant_fwd_s8_f16_outer8192_axis8192_g128": ("dqfwd", 8192, 8192, 128),
@@ -54,6 +61,7 @@ DEFAULT_CONFIG = "qkv_decode_m1_k4096_n4096"
 METRIC = "W4A16 QKV TFLOP/s and weight GB/s (1xGB300) as % of roofline"
 METRICS = {
     "qkv": METRIC,
+    "qkv8": "W8A16 QKV TFLOP/s and weight GB/s (1xGB300) as % of roofline",
     "matmul": "dense f16 tensor-core matmul fwd+bwd TFLOP/s",
     "matmul16": "dense f16 tensor-core matmul fwd+bwd, f16 results, TFLOP/s",
     "dqbwd": "per-group dequantisation backward GB/s (dy + scale read, dx written)",
@@ -72,6 +80,12 @@ L2_BYTES = 129 * 1024 * 1024
 def qkv_bytes(m, n, k):
     weights = 3 * (k // 8) * n * 4 + 3 * (k // 128) * n * 2     # packed + scales
     other = m * k * 2 + 3 * m * n * 2                             # x in, q/k/v out
+    return weights, other
+
+
+def qkv8_bytes(m, n, k):
+    weights = 3 * (k // 4) * n * 4                                # packed INT8 words
+    other = m * k * 2 + 3 * m * n * 2
     return weights, other
 
 
@@ -280,6 +294,33 @@ def run_kaio(args, cfg_name, ws, rank, local, dist):
             kernel_file = "tc_kernels.cu"
         bound = "hbm" if M <= 16 else "tensor"
         launches_per_step = 1
+    elif kind == "qkv8":
+        from qkv_projection_gb300.inputs import qkv_int8_inputs, weight_sets_int8
+        wbytes, obytes = qkv8_bytes(M, N, K)
+        inp = qkv_int8_inputs(M, N, K, seed=0)
+        nsets = max(2, -(-3 * L2_BYTES // wbytes))
+        sets = [tuple(dev(w) for w in inp.weights())]
+        for ws_ in weight_sets_int8(N, K, nsets - 1, seed=1):
+            sets.append(tuple(dev(w) for w in ws_))
+        x = dev(inp.x)
+        outs = [torch.empty((M, N), dtype=torch.float16, device=device) for _ in range(3)]
+        lib = kaio.lib()
+        ptr_sets = [[t.data_ptr() for t in s_] for s_ in sets]
+        xo = [x.data_ptr()] + [o.data_ptr() for o in outs]
+        sc = inp.scales()
+        sp = int(stream.cuda_stream)
+
+        def step(i):
+            w = ptr_sets[i % len(ptr_sets)]
+            kaio.check(lib.kaio_qkv_project_int8(xo[0], w[0], w[1], w[2], sc[0], sc[1], sc[2],
+                                                 xo[1], xo[2], xo[3], M, N, K, sp))
+
+        units_bytes = wbytes
+        alg_bytes = wbytes + obytes
+        flops = qkv_flops(M, N, K)
+        kernel_file = "tc_decode.cu" if M <= 16 else "tc_kernels.cu"
+        bound = "hbm" if M <= 16 else "tensor"
+        launches_per_step = 1
     elif kind in DEQUANT_TYPES:
         from qkv_projection_gb300.inputs import dequant_group_inputs
         outer, axis, group = M, N, K
@@ -348,7 +389,7 @@ def run_kaio(args, cfg_name, ws, rank, local, dist):
     stream.synchronize()
 
     # Capture up to `chunk` steps in one CUDA graph; replay it to cover K steps.
-    chunk = min(args.steps, 1000 if kind == "qkv" else 8)
+    chunk = min(args.steps, 1000 if kind in ("qkv", "qkv8") else 8)
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.stream(stream):
         with torch.cuda.graph(graph, stream=stream):
@@ -427,7 +468,7 @@ def run_kaio(args, cfg_name, ws, rank, local, dist):
                 "frac": round(achieved / tc_peak, 4), "peak_source": peak_src + " bf16 burst (f16 = bf16 rate)"}
     roof["traffic"] = profile_traffic(kernel_file, cfg_name)
 
-    if kind == "qkv":
+    if kind in ("qkv", "qkv8"):
         value = ws * wbytes / per_step_s / 1e9
         unit = "GB/s"
     elif kind in DEQUANT_TYPES:
@@ -437,11 +478,12 @@ def run_kaio(args, cfg_name, ws, rank, local, dist):
         value = ws * flops / per_step_s / 1e12
         unit = "TFLOP/s"
     metric = METRICS[kind]
-    dtype = {"qkv": "f16 (int4 weights, f32 accumulate)", "matmul": "f16 (f32 accumulate)",
+    dtype = {"qkv": "f16 (int4 weights, f32 accumulate)", "qkv8": "f16 (int8 weights, f32 accumulate)", "matmul": "f16 (f32 accumulate)",
              "matmul16": "f16 (f32 accumulate, f16 results)",
              "dqbwd": "bf16 (products exact in f32, rounded once)",
              "dqfwd": "int8 -> f16 (products exact in f32, rounded once)"}[kind]
     l2 = {"qkv": "inputs larger than L2 (weight sets rotated)",
+          "qkv8": "inputs larger than L2 (weight sets rotated)",
           "dqbwd": "two input/output sets of 2x128 MiB alternated (inputs larger than L2)",
           "dqfwd": "two input/output sets of 64+128 MiB alternated (inputs larger than L2)"}.get(
               kind, "operands 32 MiB each; no flush (compute-bound)")
@@ -458,11 +500,11 @@ def run_kaio(args, cfg_name, ws, rank, local, dist):
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": dtype,
-        "data": "synthetic (seeded; weights rotate over sets totalling >= 3x L2)" if kind == "qkv" else
+        "data": "synthetic (seeded; weights rotate over sets totalling >= 3x L2)" if kind in ("qkv", "qkv8") else
                 "synthetic (seeded)",
         "config": {"workload": cfg_name, **shape, "parallelism": f"replicas x{ws}", "l2": l2},
         "tflops": round(ws * flops / per_step_s / 1e12, 3) if kind not in DEQUANT_TYPES else None,
-        "weight_gbs": round(ws * wbytes / per_step_s / 1e9, 3) if kind == "qkv" else None,
+        "weight_gbs": round(ws * wbytes / per_step_s / 1e9, 3) if kind in ("qkv", "qkv8") else None,
         "roofline": roof,
         "e2e": e2e,
         "gpu_launches": steps * launches_per_step,
@@ -484,6 +526,15 @@ def oracle_step_fn(cfg_name, frac):
     kind, M, N, K = CONFIGS[cfg_name]
     if kind in DEQUANT_TYPES:
         return dequant_oracle_step_fn(cfg_name, frac)
+    if kind == "qkv8":
+        from qkv_projection_gb300.inputs import qkv_int8_inputs
+        inp8 = qkv_int8_inputs(M, N, K, seed=0)
+        ncols = max(8, int(round(N * frac)) // 8 * 8)
+        ws8 = [np.ascontiguousarray(w[:, :ncols]) for w in inp8.weights()]
+
+        def step8():
+            oracle.qkv_project_int8_ref(inp8.x, *ws8, *inp8.scales())
+        return step8, qkv8_bytes(M, ncols, K)[0], ncols
     inp = qkv_inputs(M, N, K, seed=0)
     ncols = max(8, int(round(N * frac)) // 8 * 8)
     cols = np.arange(ncols)

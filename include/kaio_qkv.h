@@ -113,6 +113,40 @@ int kaio_qkv_project_int4_noalloc(const void* x, const uint32_t* wq, const uint3
                                   uint32_t N, uint32_t K, kaio_stream_t stream);
 
 /*
+ * W8A16 fused tri-output QKV projection, the INT8 sibling of
+ * kaio_qkv_project_int4. ("kaio-candle -- src/qkv_project_int4.rs", module
+ * doc: the INT4 op follows the INT8 op's direct-call pattern but takes seven
+ * tensors, three of them group scales; both return f16 converted in-kernel
+ * from f32.) The pages show no more of the INT8 op; this entry states its
+ * contract as the INT4 layout with 8-bit fields and no group-scale tensors:
+ *
+ * For p in {q, k, v}:
+ *   out_p[m, n] = f16( scale_p * sum_{k<K} x[m, k] * int8(W_p[k, n]) ),
+ * products and sum in f32 (exact int8 -> f16 operands on the tensor cores),
+ * the scale applied to the f32 sum, rounded to f16 (nearest even) in-kernel.
+ *
+ *   x          f16  [M, K]      activations, shared by the three projections
+ *   wq, wk, wv u32  [K/4, N]    packed INT8 weights: byte i (bits 8i..8i+7) of
+ *                               word [r, n] is the signed two's-complement
+ *                               weight of K-row 4r+i, column n ([-128, 127])
+ *   scale_q, scale_k, scale_v   f32 by value: one scale per projection
+ *   q, k, v    f16  [M, N]      outputs; every element is written
+ *
+ * Errors (KAIO_ERR_INVALID_VALUE unless noted): a null pointer; K not a
+ * multiple of 128 (the kernels' K group); N not a multiple of 8; an output
+ * overlapping an input or another output; a pointer not on the current
+ * device; misaligned pointer (KAIO_ERR_MISALIGNED). Scales are not checked:
+ * an infinite or NaN scale gives infinite or NaN outputs.
+ *
+ * Path: M <= 16 runs the tcgen05 decode kernel (split over K across a
+ * thread-block cluster; no workspace, no allocation); larger M runs the
+ * tcgen05 tile kernel. Both read the caller's buffers only.
+ */
+int kaio_qkv_project_int8(const void* x, const uint32_t* wq, const uint32_t* wk, const uint32_t* wv,
+                          float scale_q, float scale_k, float scale_v, void* q, void* k, void* v,
+                          uint32_t M, uint32_t N, uint32_t K, kaio_stream_t stream);
+
+/*
  * Dense tensor-core matmul C = A @ B.
  * ("kaio-candle 0.2.0 -- src/matmul_tc_async.rs", module doc and
  * MatmulTcAsyncOp::cuda_fwd: f16 x f16 -> f32, inner dimensions must match.)

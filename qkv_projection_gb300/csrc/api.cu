@@ -301,6 +301,56 @@ int kaio_qkv_project_int4(const void* x, const uint32_t* wq, const uint32_t* wk,
   return KAIO_OK;
 }
 
+int kaio_qkv_project_int8(const void* x, const uint32_t* wq, const uint32_t* wk, const uint32_t* wv,
+                          float scale_q, float scale_k, float scale_v, void* q, void* k, void* v,
+                          uint32_t M, uint32_t N, uint32_t K, kaio_stream_t stream_) {
+  g_last_error.clear();
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  const size_t m = M, n = N, kk = K;
+  const Span in[4] = {{"x", x, m * kk * 2},
+                      {"w_q_packed", wq, kk / 4 * n * 4},
+                      {"w_k_packed", wk, kk / 4 * n * 4},
+                      {"w_v_packed", wv, kk / 4 * n * 4}};
+  const Span out[3] = {{"q", q, m * n * 2}, {"k", k, m * n * 2}, {"v", v, m * n * 2}};
+  KAIO_TRY(check_not_null(in, 4));
+  KAIO_TRY(check_not_null(out, 3));
+  if (K % 128 != 0)
+    return fail(KAIO_ERR_INVALID_VALUE, "K (%u) must be a multiple of 128 (the kernels' K group)", K);
+  if (N % 8 != 0)
+    return fail(KAIO_ERR_INVALID_VALUE, "N (%u) must be a multiple of 8 (16-byte rows)", N);
+  KAIO_TRY(check_aligned(in, 4));
+  KAIO_TRY(check_aligned(out, 3));
+  if (static_cast<uint64_t>(K) / 4 * N > 0x7FFFFFFFull || static_cast<uint64_t>(M) * K > (1ull << 40))
+    return fail(KAIO_ERR_INVALID_VALUE, "problem too large (M=%u N=%u K=%u)", M, N, K);
+  KAIO_TRY(check_overlap(in, 4, out, 3));
+  int dev;
+  DeviceInfo info;
+  KAIO_TRY(current_device(&dev, &info));
+  if (M == 0 || N == 0) return KAIO_OK;
+  KAIO_TRY(check_on_device(out, 3, dev));
+  if (K == 0) return zero_outputs(out, 3, stream);
+  KAIO_TRY(check_on_device(in, 4, dev));
+
+  const uint32_t* w3[3] = {wq, wk, wv};
+  const float sc3[3] = {scale_q, scale_k, scale_v};
+  __half* o3[3] = {static_cast<__half*>(q), static_cast<__half*>(k), static_cast<__half*>(v)};
+  cudaError_t e;
+  if (kaio_qkv_path(M) == 0) {
+    const kaio::TcDecodePlan tp = kaio::plan_tc_decode_int8(static_cast<int>(M), static_cast<int>(N),
+                                                            static_cast<int>(K), dev);
+    if (tp.ok) {
+      e = kaio::launch_tc_decode_int8(static_cast<const __half*>(x), w3, sc3, o3, static_cast<int>(M),
+                                      static_cast<int>(N), static_cast<int>(K), tp, stream);
+      if (e != cudaSuccess) return cuda_fail(e, "tcgen05 W8A16 decode kernel launch");
+      return KAIO_OK;
+    }
+  }
+  e = kaio::launch_tc_w8a16(static_cast<const __half*>(x), w3, sc3, o3, static_cast<int>(M),
+                            static_cast<int>(N), static_cast<int>(K), info.sms, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "tcgen05 W8A16 kernel launch");
+  return KAIO_OK;
+}
+
 int kaio_qkv_project_int4_noalloc(const void* x, const uint32_t* wq, const uint32_t* wk,
                                   const uint32_t* wv, const void* sq, const void* sk, const void* sv,
                                   void* q, void* k, void* v, uint32_t M, uint32_t N, uint32_t K,

@@ -382,6 +382,21 @@ __device__ __forceinline__ void dequant_natural(uint32_t word, uint32_t s2, uint
   out[3] = hmul2_rn(hsub2_rn(and_xor<kMixMask>(b32, kMixMagic), kMixMagic), s2);  // n6, n7
 }
 
+// ---------------------------------------------------------------------------
+// INT8 -> f16, exact (every int8 value is an f16 integer).
+//
+// Packed word P holds four signed two's-complement bytes; byte i (bits
+// 8i..8i+7) is K-row 4r+i. Exponent-bias conversion: flip each byte's sign
+// bit (u = b + 128 in 0..255), place u in the low mantissa bits of the f16
+// 1024.0 with a byte permute (bit pattern 0x6400 | u, value 1024 + u) and
+// subtract 1152 = 1024 + 128 (0x6480), an exact f16 subtraction here.
+// lo = {row 4r, row 4r+1}, hi = {row 4r+2, row 4r+3} (K-rows in memory order).
+__device__ __forceinline__ void int8x4_to_half2x2(uint32_t word, uint32_t& lo, uint32_t& hi) {
+  const uint32_t u = word ^ 0x80808080u;
+  lo = hsub2_rn(prmt(u, 0x64646464u, 0x5140u), 0x64806480u);   // bytes {u0, 0x64, u1, 0x64}
+  hi = hsub2_rn(prmt(u, 0x64646464u, 0x5342u), 0x64806480u);   // bytes {u2, 0x64, u3, 0x64}
+}
+
 __device__ __forceinline__ uint32_t half2_bits(uint16_t lo, uint16_t hi) {
   return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
 }

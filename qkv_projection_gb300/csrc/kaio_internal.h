@@ -82,6 +82,12 @@ TcDecodePlan plan_tc_decode(int M, int N, int K, int dev);
 cudaError_t launch_tc_decode(const __half* x, const uint32_t* const w[3], const __half* const s[3],
                              __half* const out[3], int M, int N, int K, const TcDecodePlan& pl,
                              cudaStream_t stream);
+// The same kernel for INT8 weights u32[K/4, N] (byte i = K-row 4r+i) with
+// one f32 scale per projection.
+TcDecodePlan plan_tc_decode_int8(int M, int N, int K, int dev);
+cudaError_t launch_tc_decode_int8(const __half* x, const uint32_t* const w[3], const float scale[3],
+                                  __half* const out[3], int M, int N, int K, const TcDecodePlan& pl,
+                                  cudaStream_t stream);
 unsigned read_and_clear_tc_decode_errors();
 
 // ------------------------------------------------- per-group dequantisation
@@ -108,6 +114,11 @@ cudaError_t launch_tc_gemm(const void* a, const void* b, void* c, GemmShape sh, 
 
 // W4A16 fused projection for M >= 17 on tcgen05 (weights as the TMEM operand).
 cudaError_t launch_tc_w4a16(const __half* x, const uint32_t* const w[3], const __half* const s[3],
+                            __half* const out[3], int M, int N, int K, int num_sms,
+                            cudaStream_t stream);
+// W8A16 prefill: packed INT8 weights u32[K/4, N] (byte i = K-row 4r+i), one
+// f32 scale per projection.
+cudaError_t launch_tc_w8a16(const __half* x, const uint32_t* const w[3], const float scale[3],
                             __half* const out[3], int M, int N, int K, int num_sms,
                             cudaStream_t stream);
 

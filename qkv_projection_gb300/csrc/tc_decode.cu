@@ -47,8 +47,6 @@ constexpr int DM = 16;                   // padded batch rows (MMA N)
 constexpr int DGPS = 2;                          // K groups (of 128 K) per shared-memory stage
 constexpr int DXBOX = DM * 64 * 2;               // one 64-K x box, 16 rows, 128B-swizzled: 2 KB
 constexpr int DX_STAGE = DGPS * 2 * DXBOX;       // 8 KB
-constexpr int DW_BOX = DGPS * 16 * DN * 4;       // 32 packed rows x 128 columns: 16 KB
-constexpr int DSTAGE_BYTES = DX_STAGE + 3 * DW_BOX;   // 56 KB, multiple of 1024
 constexpr int DMAX_STAGES = 4;
 constexpr int DSCALE_ROW = 3 * DN * 2;           // the three scale rows of one K group: 768 B
 constexpr int DDQ_WARPS = 8;                     // 2 per TMEM lane quadrant
@@ -61,12 +59,22 @@ constexpr uint32_t DA_STAGE_COLS = 192;          // 3 projections x 64 columns (
 constexpr int DRED_BYTES = 3 * DM * DN * 4;      // one CTA's partial tile (24 KB)
 constexpr int DSMEM_LIMIT = 232448 - 1024;       // opt-in per-block limit minus static shared memory
 constexpr size_t DSMEM = DSMEM_LIMIT;
-static_assert(DSTAGE_BYTES % 1024 == 0, "x boxes stay 1024-aligned");
-static_assert(DRED_BYTES <= DSTAGE_BYTES, "partials reuse the ring");
 static_assert(DA_COL0 + DASTAGES * DA_STAGE_COLS <= DTMEM_COLS, "TMEM layout");
+
+// Stage layout of one weight format (kBits = 4: INT4 with f16 group scales;
+// kBits = 8: INT8 with one f32 scale per projection, applied in the epilogue).
+template <int kBits>
+struct DFmt {
+  static constexpr int kRows = 128 * kBits / 32;        // packed rows per K group: 16 or 32
+  static constexpr int kWBox = DGPS * kRows * DN * 4;   // one projection's words per stage: 16 or 32 KB
+  static constexpr int kStage = DX_STAGE + 3 * kWBox;   // 56 or 104 KB
+  static_assert(kStage % 1024 == 0, "x boxes stay 1024-aligned");
+  static_assert(DRED_BYTES <= kStage, "partials reuse the ring");
+};
 
 struct DecTcParams {
   __half* out[3];
+  float scale[3];  // INT8: per-projection scales
   int M, N, K;
   int tiles;     // ceil(N / 128) column tiles (each covers Q, K and V)
   int S;         // cluster size: K ranges per column tile
@@ -89,11 +97,14 @@ __device__ __forceinline__ void permute_x_chunk(unsigned char* p) {
   *reinterpret_cast<uint4*>(p) = o;
 }
 
+template <int kBits>
 __global__ void __launch_bounds__(DTHREADS, 1)
     tc_decode_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW0,
                      const __grid_constant__ CUtensorMap tmW1, const __grid_constant__ CUtensorMap tmW2,
                      const __grid_constant__ CUtensorMap tmS0, const __grid_constant__ CUtensorMap tmS1,
                      const __grid_constant__ CUtensorMap tmS2, const DecTcParams p) {
+  using F = DFmt<kBits>;
+  constexpr int DW_BOX = F::kWBox, DSTAGE_BYTES = F::kStage;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = align_smem_1024(smem_raw);
   __shared__ __align__(8) uint64_t full[DMAX_STAGES], empty[DMAX_STAGES], sbar0, sbar, a_full[DASTAGES],
@@ -119,15 +130,15 @@ __global__ void __launch_bounds__(DTHREADS, 1)
   uint32_t fills[DMAX_STAGES] = {0, 0, 0, 0};
   int pst = 0, pi = 0;
   uint32_t pph = 0;
-  const int nsb = (nsg + p.sbox - 1) / p.sbox;             // boxes of scale rows
+  const int nsb = kBits == 4 ? (nsg + p.sbox - 1) / p.sbox : 0;   // boxes of scale rows
   auto issue_stage = [&]() {
     unsigned char* sx = smem + pst * DSTAGE_BYTES;
     unsigned char* sw = sx + DX_STAGE;
     const int g = g_begin + pi * DGPS;
     mbar_arrive_expect_tx(&full[pst], DSTAGE_BYTES);
-    tma_load_2d(sw, &tmW0, &full[pst], n0, g * 16);
-    tma_load_2d(sw + DW_BOX, &tmW1, &full[pst], n0, g * 16);
-    tma_load_2d(sw + 2 * DW_BOX, &tmW2, &full[pst], n0, g * 16);
+    tma_load_2d(sw, &tmW0, &full[pst], n0, g * F::kRows);
+    tma_load_2d(sw + DW_BOX, &tmW1, &full[pst], n0, g * F::kRows);
+    tma_load_2d(sw + 2 * DW_BOX, &tmW2, &full[pst], n0, g * F::kRows);
 #pragma unroll
     for (int b = 0; b < 2 * DGPS; ++b)
       tma_load_2d(sx + b * DXBOX, &tmX, &full[pst], (g * 2 + b) * 64, 0);
@@ -160,7 +171,9 @@ __global__ void __launch_bounds__(DTHREADS, 1)
     grid_dependency_wait();                       // the previous kernel's writes are visible
     tma_prefetch_desc(&tmX);
     tma_prefetch_desc(&tmW0); tma_prefetch_desc(&tmW1); tma_prefetch_desc(&tmW2);
-    tma_prefetch_desc(&tmS0); tma_prefetch_desc(&tmS1); tma_prefetch_desc(&tmS2);
+    if (kBits == 4) {
+      tma_prefetch_desc(&tmS0); tma_prefetch_desc(&tmS1); tma_prefetch_desc(&tmS2);
+    }
     if (nstg > 0) issue_stage();
     if (nsb > 0) {
       mbar_arrive_expect_tx(&sbar0, static_cast<uint32_t>(3 * p.sbox * DN * 2));
@@ -226,12 +239,15 @@ __global__ void __launch_bounds__(DTHREADS, 1)
           const uint32_t acc0 = (i | j) != 0 ? 1u : 0u;
           const uint32_t abase = tmem + DA_COL0 + static_cast<uint32_t>(a * DA_STAGE_COLS + q * 64);
           const uint32_t xlo = blo + static_cast<uint32_t>((2 * j * DXBOX) >> 4);
+          // MMA step (hh, kk) covers K 64hh + 16kk .. +15 of the group: x box hh,
+          // chunk kk; its A columns are kk*16 + hh*8 (INT4: the dequant warps'
+          // interleaved order) or 32hh + 8kk (INT8: K pairs in order).
 #pragma unroll
           for (int hh = 0; hh < 2; ++hh)
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              umma_ts_lohi(dq, abase + kk * 16 + hh * 8, xlo + ((hh * DXBOX + kk * 32) >> 4), bhi, idesc,
-                           (hh | kk) != 0 ? 1u : acc0);
+              umma_ts_lohi(dq, abase + (kBits == 4 ? kk * 16 + hh * 8 : hh * 32 + kk * 8),
+                           xlo + ((hh * DXBOX + kk * 32) >> 4), bhi, idesc, (hh | kk) != 0 ? 1u : acc0);
           umma_commit(&a_empty[a]);
           if (j == ngs - 1) umma_commit(&empty[st]);
         }
@@ -274,10 +290,38 @@ __global__ void __launch_bounds__(DTHREADS, 1)
       const int ngs = min(DGPS, nsg - i * DGPS);
       if (js < ngs) {
         if (!mbar_wait(&full[st], ph, abort, &g_td_err)) { ok = false; break; }
-        if (pm < p.M) {
+        if (kBits == 4 && pm < p.M) {
           permute_x_chunk(smem + st * DSTAGE_BYTES + poff);
           permute_x_chunk(smem + st * DSTAGE_BYTES + poff + DXBOX);
           fence_proxy_async_smem();               // the MMAs read x through the async proxy
+        }
+        if constexpr (kBits == 8) {
+          // Thread = column nl: its 32 packed rows of the group per projection,
+          // converted exactly to f16 K pairs. Column c of projection q's 64 holds
+          // K pair c (K-rows 2c, 2c+1: byte pair c % 2 of packed row c / 2).
+          if (!mbar_wait(&a_empty[js], aph ^ 1, abort, &g_td_err)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t* sw = reinterpret_cast<const uint32_t*>(smem + st * DSTAGE_BYTES + DX_STAGE) +
+                               js * F::kRows * DN + nl;
+#pragma unroll
+          for (int q = 0; q < 3; ++q)
+#pragma unroll
+            for (int k2 = 0; k2 < 2; ++k2) {
+              uint32_t v[32];
+#pragma unroll
+              for (int rr = 0; rr < 16; ++rr)
+                int8x4_to_half2x2(sw[q * (DW_BOX / 4) + (k2 * 16 + rr) * DN], v[2 * rr], v[2 * rr + 1]);
+              tmem_st32(tbase + q * 64 + k2 * 32, v);
+            }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&empty[st]);   // this set's words of the stage have been read
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&a_full[js]);
+          aph ^= 1;
+          if (++st == p.nst) { st = 0; ph ^= 1; }
+          continue;
         }
         const int gl = i * DGPS + js;             // group index inside the CTA's range
         if (!have_scales && gl >= p.sbox) {
@@ -377,6 +421,10 @@ __global__ void __launch_bounds__(DTHREADS, 1)
         if (r < p.S) {
           acc.x += v[r].x; acc.y += v[r].y; acc.z += v[r].z; acc.w += v[r].w;
         }
+      if (kBits == 8) {
+        const float sc = q == 0 ? p.scale[0] : (q == 1 ? p.scale[1] : p.scale[2]);
+        acc.x *= sc; acc.y *= sc; acc.z *= sc; acc.w *= sc;
+      }
       const int c4 = n0 + 4 * n4;
       if (c4 < p.N) {
         __half* out = q == 0 ? p.out[0] : (q == 1 ? p.out[1] : p.out[2]);
@@ -398,6 +446,7 @@ __global__ void __launch_bounds__(DTHREADS, 1)
   }
 }
 
+template <int kBits>
 int dec_max_active_clusters(int S, int dev) {
   static std::mutex mu;
   static std::map<std::pair<int, int>, int> cache;
@@ -406,7 +455,7 @@ int dec_max_active_clusters(int S, int dev) {
   auto it = cache.find(key);
   if (it != cache.end()) return it->second;
   int n = 0;
-  const void* kern = reinterpret_cast<const void*>(tc_decode_kernel);
+  const void* kern = reinterpret_cast<const void*>(tc_decode_kernel<kBits>);
   if (ensure_smem_limit(kern, static_cast<int>(DSMEM)) == cudaSuccess) {
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(static_cast<unsigned>(S * 64));
@@ -428,18 +477,17 @@ int dec_max_active_clusters(int S, int dev) {
   return n;
 }
 
-}  // namespace
-
-TcDecodePlan plan_tc_decode(int M, int N, int K, int dev) {
+template <int kBits>
+TcDecodePlan plan_dec(int M, int N, int K, int dev) {
   TcDecodePlan pl{};
   pl.tiles = (N + DN - 1) / DN;
   pl.ng = K / 128;
   double best = -1;
   for (int S = 1; S <= 8 && S <= pl.ng; ++S) {
     const int range = (pl.ng + S - 1) / S;
-    const int sbytes = ((range + 7) / 8) * 8 * DSCALE_ROW;
-    if (sbytes + 2 * DSTAGE_BYTES + 2048 > DSMEM_LIMIT) continue;   // scales + 2 stages must fit
-    const int slots = dec_max_active_clusters(S, dev);
+    const int sbytes = kBits == 4 ? ((range + 7) / 8) * 8 * DSCALE_ROW : 0;
+    if (sbytes + 2 * DFmt<kBits>::kStage + 2048 > DSMEM_LIMIT) continue;   // scales + 2 stages must fit
+    const int slots = dec_max_active_clusters<kBits>(S, dev);
     if (slots <= 0) continue;
     const long long waves = (pl.tiles + slots - 1) / slots;
     // Cost: K groups the busiest SM streams, plus a fixed start-up cost per wave.
@@ -453,14 +501,21 @@ TcDecodePlan plan_tc_decode(int M, int N, int K, int dev) {
   return pl;
 }
 
-cudaError_t launch_tc_decode(const __half* x, const uint32_t* const w[3], const __half* const s[3],
-                             __half* const out[3], int M, int N, int K, const TcDecodePlan& pl,
-                             cudaStream_t stream) {
+// s: INT4 group scales (kBits = 4, else unused); scale: INT8 per-projection
+// scales (kBits = 8, else unused).
+template <int kBits>
+cudaError_t launch_dec(const __half* x, const uint32_t* const w[3], const __half* const s[3],
+                       const float* scale, __half* const out[3], int M, int N, int K,
+                       const TcDecodePlan& pl, cudaStream_t stream) {
+  using F = DFmt<kBits>;
   const int range = (pl.ng + pl.S - 1) / pl.S;
-  const int sbox = std::min(8, pl.ng);
-  const int sbytes = ((range + sbox - 1) / sbox) * sbox * DSCALE_ROW;
+  const int sbox = kBits == 4 ? std::min(8, pl.ng) : 1;
+  const int sbytes = kBits == 4 ? ((range + sbox - 1) / sbox) * sbox * DSCALE_ROW : 0;
   DecTcParams p{};
-  for (int q = 0; q < 3; ++q) p.out[q] = out[q];
+  for (int q = 0; q < 3; ++q) {
+    p.out[q] = out[q];
+    p.scale[q] = kBits == 8 ? scale[q] : 1.f;
+  }
   p.M = M;
   p.N = N;
   p.K = K;
@@ -469,23 +524,28 @@ cudaError_t launch_tc_decode(const __half* x, const uint32_t* const w[3], const 
   p.ng = pl.ng;
   p.sbox = sbox;
   const int nstg = (range + DGPS - 1) / DGPS;
-  p.nst = std::min(std::min(nstg, DMAX_STAGES), (DSMEM_LIMIT - 1024 - sbytes) / DSTAGE_BYTES);
+  p.nst = std::min(std::min(nstg, DMAX_STAGES), (DSMEM_LIMIT - 1024 - sbytes) / F::kStage);
   p.nst = std::max(p.nst, 1);
-  p.s_off = p.nst * DSTAGE_BYTES;
+  p.s_off = p.nst * F::kStage;
   const size_t smem_used = static_cast<size_t>(p.s_off + sbytes + 1024);
   CUtensorMap tx, tw[3], ts[3];
   CUresult r = encode_tensor_map_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, x, K, M,
                                     static_cast<uint64_t>(K) * 2, 64, DM, CU_TENSOR_MAP_SWIZZLE_128B);
   if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   for (int q = 0; q < 3; ++q) {
-    r = encode_tensor_map_2d(&tw[q], CU_TENSOR_MAP_DATA_TYPE_UINT32, w[q], N, K / 8,
-                             static_cast<uint64_t>(N) * 4, DN, DGPS * 16, CU_TENSOR_MAP_SWIZZLE_NONE);
+    r = encode_tensor_map_2d(&tw[q], CU_TENSOR_MAP_DATA_TYPE_UINT32, w[q], N, K * kBits / 32,
+                             static_cast<uint64_t>(N) * 4, DN, DGPS * F::kRows, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-    r = encode_tensor_map_2d(&ts[q], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, s[q], N, K / 128,
-                             static_cast<uint64_t>(N) * 2, DN, sbox, CU_TENSOR_MAP_SWIZZLE_NONE);
-    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    if (kBits == 4) {
+      r = encode_tensor_map_2d(&ts[q], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, s[q], N, K / 128,
+                               static_cast<uint64_t>(N) * 2, DN, sbox, CU_TENSOR_MAP_SWIZZLE_NONE);
+      if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    } else {
+      ts[q] = tx;   // not read by the INT8 kernel
+    }
   }
-  cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(tc_decode_kernel), static_cast<int>(DSMEM));
+  cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(tc_decode_kernel<kBits>),
+                                    static_cast<int>(DSMEM));
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(static_cast<unsigned>(pl.tiles * pl.S));
@@ -506,9 +566,27 @@ cudaError_t launch_tc_decode(const __half* x, const uint32_t* const w[3], const 
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  e = cudaLaunchKernelEx(&cfg, tc_decode_kernel, tx, tw[0], tw[1], tw[2], ts[0], ts[1], ts[2], p);
+  e = cudaLaunchKernelEx(&cfg, tc_decode_kernel<kBits>, tx, tw[0], tw[1], tw[2], ts[0], ts[1], ts[2], p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
+}
+
+}  // namespace
+
+TcDecodePlan plan_tc_decode(int M, int N, int K, int dev) { return plan_dec<4>(M, N, K, dev); }
+TcDecodePlan plan_tc_decode_int8(int M, int N, int K, int dev) { return plan_dec<8>(M, N, K, dev); }
+
+cudaError_t launch_tc_decode(const __half* x, const uint32_t* const w[3], const __half* const s[3],
+                             __half* const out[3], int M, int N, int K, const TcDecodePlan& pl,
+                             cudaStream_t stream) {
+  return launch_dec<4>(x, w, s, nullptr, out, M, N, K, pl, stream);
+}
+
+cudaError_t launch_tc_decode_int8(const __half* x, const uint32_t* const w[3], const float scale[3],
+                                  __half* const out[3], int M, int N, int K, const TcDecodePlan& pl,
+                                  cudaStream_t stream) {
+  const __half* none[3] = {nullptr, nullptr, nullptr};
+  return launch_dec<8>(x, w, none, scale, out, M, N, K, pl, stream);
 }
 
 unsigned read_and_clear_tc_decode_errors() {

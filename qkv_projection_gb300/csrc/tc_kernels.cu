@@ -5,8 +5,11 @@
 //    dA = grad * B^T, dB = A^T * grad of MatmulTcAsyncOp::bwd, taken here by
 //    reading the stored operands in the other major order instead of copying
 //    transposes).
-//  * tc_w4a16_kernel: the W4A16 fused QKV projection of
-//    "kaio-candle -- src/qkv_project_int4.rs" for M >= 17.
+//  * tc_qkv_prefill_kernel<4>: the W4A16 fused QKV projection of
+//    "kaio-candle -- src/qkv_project_int4.rs" for M >= 17;
+//    tc_qkv_prefill_kernel<8>: its INT8 sibling (W8A16), named in the module
+//    doc of that page; INT4 packing with 8-bit fields and one f32 scale per
+//    projection, applied to the f32 accumulator in the epilogue.
 //
 // Both share one pipeline shape: a TMA producer warp fills a ring of shared
 // memory stages, a single thread issues tcgen05.mma into f32 accumulators in
@@ -17,7 +20,7 @@
 // 128 x 256 output tile; two accumulator buffers so the epilogue of one tile
 // overlaps the main loop of the next.
 //
-// W4A16: the product is computed transposed, D_p[n, m] = Wd_p^T[n, :] x^T[:, m],
+// W4A16 / W8A16: the product is computed transposed, D_p[n, m] = Wd_p^T[n, :] x^T[:, m],
 // so that the dequantised weights are the MMA's A operand and can live in
 // tensor memory: eight dequant warps read packed words from the staged tile,
 // build f16 operands in registers and write them to TMEM with tcgen05.st; the
@@ -225,29 +228,40 @@ constexpr int PBN = 128;                 // output columns per tile (MMA M)
 constexpr int PBK = 64;                  // K per TMA stage
 constexpr int PSTAGES = 4;
 constexpr int PX_BYTES = PBM * PBK * 2;          // 16384
-constexpr int PW_BYTES = (PBK / 8) * PBN * 4;    // 4096 per projection
-constexpr int PS_BYTES = PBN * 2;                // 256 per projection
-constexpr int PTX_BYTES = PX_BYTES + 3 * PW_BYTES + 3 * PS_BYTES;  // bytes landed per stage
-constexpr int PSTAGE_BYTES = 30720;              // padded to keep x tiles 1024-aligned
 constexpr int PTHREADS = 320;                    // w0 TMA, w1 MMA, w2..9 dequant + epilogue
 constexpr int PDQ_WARPS = 8;
 constexpr uint32_t PTMEM_COLS = 512;
 constexpr uint32_t PA_COL0 = 384;                // A stages after the three accumulators
 constexpr uint32_t PA_STAGE_COLS = 48;           // 3 projections x 16 columns (32 K)
-constexpr size_t PSMEM = static_cast<size_t>(PSTAGES) * PSTAGE_BYTES + 1024;
-static_assert(PTX_BYTES <= PSTAGE_BYTES, "stage layout");
 
-struct W4Params {
+// Stage layout of one weight format (kBits = 4: INT4 with f16 group scales;
+// kBits = 8: INT8 with one f32 scale per projection, applied in the epilogue).
+template <int kBits>
+struct PFmt {
+  static constexpr int kRows = PBK * kBits / 32;             // packed rows per stage: 8 or 16
+  static constexpr int kWBytes = kRows * PBN * 4;            // one projection's words: 4 or 8 KB
+  static constexpr int kSBytes = kBits == 4 ? PBN * 2 : 0;   // one projection's scale row
+  static constexpr int kTx = PX_BYTES + 3 * kWBytes + 3 * kSBytes;   // bytes landed per stage
+  static constexpr int kStage = kBits == 4 ? 30720 : 40960;  // padded: x tiles stay 1024-aligned
+  static constexpr size_t kSmem = static_cast<size_t>(PSTAGES) * kStage + 1024;
+  static_assert(kTx <= kStage && kStage % 1024 == 0, "stage layout");
+};
+
+struct PrefillParams {
   __half* out[3];
+  float scale[3];        // INT8: per-projection scales
   int M, N, K;
   int m_blocks, tiles;
 };
 
+template <int kBits>
 __global__ void __launch_bounds__(PTHREADS, 1)
-    tc_w4a16_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW0,
+    tc_qkv_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW0,
                     const __grid_constant__ CUtensorMap tmW1, const __grid_constant__ CUtensorMap tmW2,
                     const __grid_constant__ CUtensorMap tmS0, const __grid_constant__ CUtensorMap tmS1,
-                    const __grid_constant__ CUtensorMap tmS2, const W4Params p) {
+                    const __grid_constant__ CUtensorMap tmS2, const PrefillParams p) {
+  using F = PFmt<kBits>;
+  constexpr int PW_BYTES = F::kWBytes, PS_BYTES = F::kSBytes, PSTAGE_BYTES = F::kStage;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = align_smem_1024(smem_raw);
   __shared__ __align__(8) uint64_t full[PSTAGES], empty[PSTAGES], a_full[2], a_empty[2],
@@ -286,7 +300,9 @@ __global__ void __launch_bounds__(PTHREADS, 1)
     if (lane == 0) {
       tma_prefetch_desc(&tmX);
       tma_prefetch_desc(&tmW0); tma_prefetch_desc(&tmW1); tma_prefetch_desc(&tmW2);
-      tma_prefetch_desc(&tmS0); tma_prefetch_desc(&tmS1); tma_prefetch_desc(&tmS2);
+      if constexpr (kBits == 4) {
+        tma_prefetch_desc(&tmS0); tma_prefetch_desc(&tmS1); tma_prefetch_desc(&tmS2);
+      }
       int st = 0;
       uint32_t ph = 0;
       uint32_t fills[PSTAGES] = {0, 0, 0, 0};
@@ -296,16 +312,18 @@ __global__ void __launch_bounds__(PTHREADS, 1)
           if (!mbar_wait(&empty[st], ph ^ 1, abort, &g_tc_err)) goto producer_done;
           ++fills[st];
           unsigned char* sx = smem + st * PSTAGE_BYTES;
-          mbar_arrive_expect_tx(&full[st], PTX_BYTES);
+          mbar_arrive_expect_tx(&full[st], F::kTx);
           tma_load_2d(sx, &tmX, &full[st], ks * PBK, m0);
           unsigned char* sw = sx + PX_BYTES;
-          unsigned char* ss = sx + PX_BYTES + 3 * PW_BYTES;
-          tma_load_2d(sw, &tmW0, &full[st], n0, ks * (PBK / 8));
-          tma_load_2d(sw + PW_BYTES, &tmW1, &full[st], n0, ks * (PBK / 8));
-          tma_load_2d(sw + 2 * PW_BYTES, &tmW2, &full[st], n0, ks * (PBK / 8));
-          tma_load_2d(ss, &tmS0, &full[st], n0, ks >> 1);
-          tma_load_2d(ss + PS_BYTES, &tmS1, &full[st], n0, ks >> 1);
-          tma_load_2d(ss + 2 * PS_BYTES, &tmS2, &full[st], n0, ks >> 1);
+          tma_load_2d(sw, &tmW0, &full[st], n0, ks * F::kRows);
+          tma_load_2d(sw + PW_BYTES, &tmW1, &full[st], n0, ks * F::kRows);
+          tma_load_2d(sw + 2 * PW_BYTES, &tmW2, &full[st], n0, ks * F::kRows);
+          if constexpr (kBits == 4) {
+            unsigned char* ss = sx + PX_BYTES + 3 * PW_BYTES;
+            tma_load_2d(ss, &tmS0, &full[st], n0, ks >> 1);
+            tma_load_2d(ss + PS_BYTES, &tmS1, &full[st], n0, ks >> 1);
+            tma_load_2d(ss + 2 * PS_BYTES, &tmS2, &full[st], n0, ks >> 1);
+          }
           if (++st == PSTAGES) { st = 0; ph ^= 1; }
         }
       }
@@ -360,8 +378,8 @@ __global__ void __launch_bounds__(PTHREADS, 1)
   } else {
     // Dequant + epilogue warps. TMEM lane group sp = warp % 4: this thread owns
     // output column n0 + 32*sp + lane (TMEM lane = A row = column). hf picks the
-    // two packed rows (16 K) of each 32-K A stage this warp fills, and the half
-    // of the x rows it drains in the epilogue.
+    // 16 K of each 32-K A stage this warp fills (two INT4 or four INT8 packed
+    // rows), and the half of the x rows it drains in the epilogue.
     const int sp = warp & 3;
     const int hf = (warp - 2) >> 2;
     const int nl = 32 * sp + lane;
@@ -379,21 +397,39 @@ __global__ void __launch_bounds__(PTHREADS, 1)
         uint32_t s2[3];
 #pragma unroll
         for (int q = 0; q < 3; ++q) {
-          const uint16_t sb = __half_as_ushort(ss[q * PBN + nl]);
-          s2[q] = half2_bits(sb, sb);
+          if constexpr (kBits == 4) {
+            const uint16_t sb = __half_as_ushort(ss[q * PBN + nl]);
+            s2[q] = half2_bits(sb, sb);
+          } else {
+            s2[q] = 0;
+          }
         }
+        (void)ss;
         for (int hh = 0; hh < 2; ++hh) {
           if (!mbar_wait(&a_empty[a], aph ^ 1, abort, &g_tc_err)) { ok = false; break; }
           tc_fence_after();
-          const int r0 = hh * 4 + hf * 2;
 #pragma unroll
           for (int q = 0; q < 3; ++q) {
-            const uint32_t w0 = sw[q * (PW_BYTES / 4) + r0 * PBN + nl];
-            const uint32_t w1 = sw[q * (PW_BYTES / 4) + (r0 + 1) * PBN + nl];
-            uint32_t v0[4], v1[4];
-            dequant_natural(w0, s2[q], v0);
-            dequant_natural(w1, s2[q], v1);
-            const uint32_t v[8] = {v0[0], v0[1], v0[2], v0[3], v1[0], v1[1], v1[2], v1[3]};
+            // column q*16 + hf*8 + c of the A stage holds K pair c of this warp's 16 K
+            uint32_t v[8];
+            if constexpr (kBits == 4) {
+              const int r0 = hh * 4 + hf * 2;
+              const uint32_t w0 = sw[q * (PW_BYTES / 4) + r0 * PBN + nl];
+              const uint32_t w1 = sw[q * (PW_BYTES / 4) + (r0 + 1) * PBN + nl];
+              uint32_t v0[4], v1[4];
+              dequant_natural(w0, s2[q], v0);
+              dequant_natural(w1, s2[q], v1);
+#pragma unroll
+              for (int c = 0; c < 4; ++c) {
+                v[c] = v0[c];
+                v[4 + c] = v1[c];
+              }
+            } else {
+              const int r0 = hh * 8 + hf * 4;
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                int8x4_to_half2x2(sw[q * (PW_BYTES / 4) + (r0 + j) * PBN + nl], v[2 * j], v[2 * j + 1]);
+            }
             tmem_st8(tmem + lane_base + PA_COL0 + a * PA_STAGE_COLS + q * 16 + hf * 8, v);
           }
           tmem_st_wait();
@@ -418,6 +454,7 @@ __global__ void __launch_bounds__(PTHREADS, 1)
 #pragma unroll 1
       for (int q = 0; q < 3; ++q) {
         __half* out = (q == 0) ? p.out[0] : (q == 1) ? p.out[1] : p.out[2];
+        const float sc = (q == 0) ? p.scale[0] : (q == 1) ? p.scale[1] : p.scale[2];
 #pragma unroll 1
         for (int mh = 0; mh < 2; ++mh) {
           const int mb = 64 * hf + 32 * mh;
@@ -426,7 +463,11 @@ __global__ void __launch_bounds__(PTHREADS, 1)
           tmem_ld_wait();
 #pragma unroll
           for (int j = 0; j < 32; j += 2) {
-            const float own_lo = __uint_as_float(r[j]), own_hi = __uint_as_float(r[j + 1]);
+            float own_lo = __uint_as_float(r[j]), own_hi = __uint_as_float(r[j + 1]);
+            if constexpr (kBits == 8) {
+              own_lo *= sc;
+              own_hi *= sc;
+            }
             const float send = odd ? own_lo : own_hi;
             const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
             const int m = m0 + mb + j + (odd ? 1 : 0);
@@ -591,24 +632,37 @@ cudaError_t launch_tc_gemm(const void* a, const void* b, void* c, GemmShape sh, 
   return cudaGetLastError();
 }
 
-cudaError_t launch_tc_w4a16(const __half* x, const uint32_t* const w[3], const __half* const s[3],
-                            __half* const out[3], int M, int N, int K, int num_sms,
-                            cudaStream_t stream) {
+namespace {
+
+// s: INT4 group scales (kBits = 4, else unused); scale: INT8 per-projection
+// scales (kBits = 8, else unused).
+template <int kBits>
+cudaError_t launch_prefill(const __half* x, const uint32_t* const w[3], const __half* const s[3],
+                           const float* scale, __half* const out[3], int M, int N, int K,
+                           int num_sms, cudaStream_t stream) {
+  using F = PFmt<kBits>;
   CUtensorMap tx, tw[3], ts[3];
   CUresult r = encode_tensor_map_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, x, K, M,
                                     static_cast<uint64_t>(K) * 2, PBK, PBM,
                                     CU_TENSOR_MAP_SWIZZLE_128B);
   if (r != CUDA_SUCCESS) return map_error(r);
   for (int q = 0; q < 3; ++q) {
-    r = encode_tensor_map_2d(&tw[q], CU_TENSOR_MAP_DATA_TYPE_UINT32, w[q], N, K / 8,
-                             static_cast<uint64_t>(N) * 4, PBN, PBK / 8, CU_TENSOR_MAP_SWIZZLE_NONE);
+    r = encode_tensor_map_2d(&tw[q], CU_TENSOR_MAP_DATA_TYPE_UINT32, w[q], N, K * kBits / 32,
+                             static_cast<uint64_t>(N) * 4, PBN, F::kRows, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (r != CUDA_SUCCESS) return map_error(r);
-    r = encode_tensor_map_2d(&ts[q], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, s[q], N, K / 128,
-                             static_cast<uint64_t>(N) * 2, PBN, 1, CU_TENSOR_MAP_SWIZZLE_NONE);
-    if (r != CUDA_SUCCESS) return map_error(r);
+    if (kBits == 4) {
+      r = encode_tensor_map_2d(&ts[q], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, s[q], N, K / 128,
+                               static_cast<uint64_t>(N) * 2, PBN, 1, CU_TENSOR_MAP_SWIZZLE_NONE);
+      if (r != CUDA_SUCCESS) return map_error(r);
+    } else {
+      ts[q] = tx;   // not read by the INT8 kernel
+    }
   }
-  W4Params p{};
-  for (int q = 0; q < 3; ++q) p.out[q] = out[q];
+  PrefillParams p{};
+  for (int q = 0; q < 3; ++q) {
+    p.out[q] = out[q];
+    p.scale[q] = kBits == 8 ? scale[q] : 1.f;
+  }
   p.M = M;
   p.N = N;
   p.K = K;
@@ -616,11 +670,27 @@ cudaError_t launch_tc_w4a16(const __half* x, const uint32_t* const w[3], const _
   const int n_blocks = (N + PBN - 1) / PBN;
   p.tiles = p.m_blocks * n_blocks;
   const int grid = std::min(p.tiles, num_sms);
-  cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(tc_w4a16_kernel),
-                                    static_cast<int>(PSMEM));
+  cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(tc_qkv_prefill_kernel<kBits>),
+                                    static_cast<int>(F::kSmem));
   if (e != cudaSuccess) return e;
-  tc_w4a16_kernel<<<grid, PTHREADS, PSMEM, stream>>>(tx, tw[0], tw[1], tw[2], ts[0], ts[1], ts[2], p);
+  tc_qkv_prefill_kernel<kBits><<<grid, PTHREADS, F::kSmem, stream>>>(tx, tw[0], tw[1], tw[2], ts[0], ts[1],
+                                                                     ts[2], p);
   return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_tc_w4a16(const __half* x, const uint32_t* const w[3], const __half* const s[3],
+                            __half* const out[3], int M, int N, int K, int num_sms,
+                            cudaStream_t stream) {
+  return launch_prefill<4>(x, w, s, nullptr, out, M, N, K, num_sms, stream);
+}
+
+cudaError_t launch_tc_w8a16(const __half* x, const uint32_t* const w[3], const float scale[3],
+                            __half* const out[3], int M, int N, int K, int num_sms,
+                            cudaStream_t stream) {
+  const __half* none[3] = {nullptr, nullptr, nullptr};
+  return launch_prefill<8>(x, w, none, scale, out, M, N, K, num_sms, stream);
 }
 
 cudaError_t launch_dequant_debug(const uint32_t* w, const __half* s, __half* out, int K, int N,

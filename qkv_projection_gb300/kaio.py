@@ -38,6 +38,7 @@ _SIGNATURES = {
     "kaio_dequant_int4_debug": ([_vp, _vp, _vp, _u32, _u32, _i32, _vp], _i32),
     "kaio_dequantize_per_group_backward": ([_i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp], _i32),
     "kaio_dequantize_per_group": ([_i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp], _i32),
+    "kaio_qkv_project_int8": ([_vp] * 4 + [ctypes.c_float] * 3 + [_vp] * 3 + [_u32, _u32, _u32, _vp], _i32),
     "kaio_qkv_path": ([_u32], _i32),
     "kaio_last_error": ([], ctypes.c_char_p),
     "kaio_device_status": ([], _i32),
@@ -152,6 +153,32 @@ def qkv_project_int4(x, w_q_packed, w_k_packed, w_v_packed, scales_q, scales_k, 
     check(lib().kaio_qkv_project_int4(
         x.data_ptr(), w_q_packed.data_ptr(), w_k_packed.data_ptr(), w_v_packed.data_ptr(),
         scales_q.data_ptr(), scales_k.data_ptr(), scales_v.data_ptr(),
+        out[0].data_ptr(), out[1].data_ptr(), out[2].data_ptr(), m, n, k, _stream_ptr(stream)))
+    return out
+
+
+def qkv_project_int8(x, w_q_packed, w_k_packed, w_v_packed, scale_q: float, scale_k: float,
+                     scale_v: float, out: Optional[Tuple] = None, stream=None):
+    """Fused W8A16 QKV projection: returns (q, k, v), each f16 [M, N].
+
+    x f16 [M, K]; w_*_packed int32/uint32 [K/4, N] (4 signed INT8 per word,
+    byte i = K-row 4r+i); scale_* one float per projection (passed as f32).
+    """
+    torch = _torch()
+    _need(x, "x", (torch.float16,))
+    m, k = x.shape
+    if k % 128:
+        raise ValueError(f"K ({k}) must be a multiple of 128")
+    n = w_q_packed.shape[1] if w_q_packed.dim() == 2 else -1
+    for name, t in (("w_q_packed", w_q_packed), ("w_k_packed", w_k_packed), ("w_v_packed", w_v_packed)):
+        _need(t, name, _packed_dtypes(), (k // 4, n))
+    if out is None:
+        out = tuple(torch.empty((m, n), dtype=torch.float16, device=x.device) for _ in range(3))
+    for name, t in zip("qkv", out):
+        _need(t, name, (torch.float16,), (m, n))
+    check(lib().kaio_qkv_project_int8(
+        x.data_ptr(), w_q_packed.data_ptr(), w_k_packed.data_ptr(), w_v_packed.data_ptr(),
+        float(scale_q), float(scale_k), float(scale_v),
         out[0].data_ptr(), out[1].data_ptr(), out[2].data_ptr(), m, n, k, _stream_ptr(stream)))
     return out
 

@@ -172,3 +172,45 @@ def test_dequant_group_validation_order(L):
     # exactly in place passes the argument checks; without a GPU it then fails on CUDA
     st = bwd(F16, S8, 2, 8, 4, dy, sc, dy, None)
     assert st != INVALID or "overlap" not in kaio.last_error()
+
+
+def qkv8(L, M=16, N=128, K=256, ptrs=None, scales=(1.0, 1.0, 1.0), stream=None):
+    p = list(ptrs) if ptrs is not None else [ptr(i) for i in range(7)]
+    return L.kaio_qkv_project_int8(*p[:4], *scales, *p[4:], M, N, K, stream)
+
+
+def test_int8_entry_validation(L):
+    for i in range(7):                                   # x, 3 weights, 3 outputs
+        p = [ptr(j) for j in range(7)]
+        p[i] = None
+        assert qkv8(L, ptrs=p) == INVALID and "null" in kaio.last_error()
+    for K in (64, 130, 200, 4):
+        assert qkv8(L, K=K) == INVALID and "multiple of 128" in kaio.last_error()
+    for N in (1, 4, 12, 130):
+        assert qkv8(L, N=N) == INVALID and "N (" in kaio.last_error()
+    for i in range(7):
+        p = [ptr(j) for j in range(7)]
+        p[i] += 8
+        assert qkv8(L, ptrs=p) == MISALIGNED
+    p = [ptr(j) for j in range(7)]
+    p[4] = p[0] + 16                                      # q overlaps x
+    assert qkv8(L, ptrs=p) == INVALID and "overlaps input x" in kaio.last_error()
+    p = [ptr(j) for j in range(7)]
+    p[6] = p[1] + 64                                      # v overlaps w_q_packed
+    assert qkv8(L, ptrs=p) == INVALID and "w_q_packed" in kaio.last_error()
+    # the packed weights are [K/4, N] words: v right after a [K/4, N] w_q is fine
+    p = [ptr(j) for j in range(7)]
+    p[6] = p[1] + 256 // 4 * 128 * 4
+    assert qkv8(L, ptrs=p) not in (INVALID, MISALIGNED)
+    # scales are passed by value and not validated
+    assert qkv8(L, scales=(float("nan"), 0.0, -1.0)) not in (INVALID, MISALIGNED)
+
+
+def test_int8_binding_checks_shapes():
+    import torch
+    x = torch.zeros(4, 128, dtype=torch.float16)
+    with pytest.raises(ValueError, match="CUDA device"):
+        w = torch.zeros(32, 8, dtype=torch.int32)
+        kaio.qkv_project_int8(x, w, w, w, 1.0, 1.0, 1.0)
+    with pytest.raises(ValueError):
+        kaio.qkv_project_int8(torch.zeros(4, 100, dtype=torch.float16), w, w, w, 1.0, 1.0, 1.0)
