@@ -152,6 +152,15 @@ __device__ __forceinline__ void allow_dependents_launch() {
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
 }
+// Bring one 2-D box of a tensor into L2 (no shared memory, no barrier). A
+// performance hint only: it loads nothing into the SM, so it may run before
+// the dependency wait on a preceding kernel -- L2 is the point of coherence,
+// and a later write by that kernel updates the cached line.
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int c0, int c1) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(map), "r"(c0),
+               "r"(c1)
+               : "memory");
+}
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar,
                                             int c0, int c1) {
   asm volatile(

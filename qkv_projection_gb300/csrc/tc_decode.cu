@@ -168,12 +168,22 @@ __global__ void __launch_bounds__(DTHREADS, 1)
     for (int w = 0; w < DMMA_WARPS; ++w) mbar_init(&mma_done[w], 1);
     abort_flag = 0;
     fence_mbar_init();
-    grid_dependency_wait();                       // the previous kernel's writes are visible
     tma_prefetch_desc(&tmX);
     tma_prefetch_desc(&tmW0); tma_prefetch_desc(&tmW1); tma_prefetch_desc(&tmW2);
     if (kBits == 4) {
       tma_prefetch_desc(&tmS0); tma_prefetch_desc(&tmS1); tma_prefetch_desc(&tmS2);
     }
+    // While the preceding kernel finishes, start pulling the weights of this
+    // CTA's first stage from HBM into L2 (hints only, see tma_prefetch_l2_2d),
+    // so that its copies after the wait find them there. Only the first stage:
+    // prefetching a CTA's whole range evicts lines before use on workloads
+    // near the L2 size, and deeper L2 look-ahead of the ring slowed M = 1.
+    if (nstg > 0) {
+      tma_prefetch_l2_2d(&tmW0, n0, g_begin * F::kRows);
+      tma_prefetch_l2_2d(&tmW1, n0, g_begin * F::kRows);
+      tma_prefetch_l2_2d(&tmW2, n0, g_begin * F::kRows);
+    }
+    grid_dependency_wait();                       // the previous kernel's writes are visible
     if (nstg > 0) issue_stage();
     if (nsb > 0) {
       mbar_arrive_expect_tx(&sbar0, static_cast<uint32_t>(3 * p.sbox * DN * 2));
