@@ -284,6 +284,10 @@ def run_kaio(args, cfg_name, ws, rank, local, dist):
             if st:
                 raise kaio.KaioError(st, kaio.last_error())
 
+        def e2e_call(i, ins):
+            return kaio.qkv_project_int4(ins[0], *sets[i % len(sets)], out=outs, stream=stream)
+        e2e_case = ([x], e2e_call, {"weights_resident": True})
+
         units_bytes = wbytes
         alg_bytes = wbytes + obytes
         flops = qkv_flops(M, N, K)
@@ -314,6 +318,10 @@ def run_kaio(args, cfg_name, ws, rank, local, dist):
             w = ptr_sets[i % len(ptr_sets)]
             kaio.check(lib.kaio_qkv_project_int8(xo[0], w[0], w[1], w[2], sc[0], sc[1], sc[2],
                                                  xo[1], xo[2], xo[3], M, N, K, sp))
+
+        def e2e_call(i, ins):
+            return kaio.qkv_project_int8(ins[0], *sets[i % len(sets)], *sc, out=outs, stream=stream)
+        e2e_case = ([x], e2e_call, {"weights_resident": True})
 
         units_bytes = wbytes
         alg_bytes = wbytes + obytes
@@ -350,6 +358,12 @@ def run_kaio(args, cfg_name, ws, rank, local, dist):
                 kaio.check(lib.kaio_dequantize_per_group(qcode, fcode, outer, axis, group, a.data_ptr(),
                                                          S.data_ptr(), o.data_ptr(), sp))
 
+        def e2e_call(i, ins):
+            if kind == "dqbwd":
+                return [kaio.dequantize_per_group_backward(ins[0], ins[1], group, out=outs[i % 2], stream=stream)]
+            return [kaio.dequantize_per_group(ins[0], ins[1], group, out=outs[i % 2], stream=stream)]
+        e2e_case = ([src, S], e2e_call, {})
+
         wbytes = 0
         units_bytes = dequant_bytes(kind, outer, axis, group)
         alg_bytes = units_bytes
@@ -373,6 +387,11 @@ def run_kaio(args, cfg_name, ws, rank, local, dist):
             kaio.check(fwd(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K, sp))
             kaio.check(bwd(A.data_ptr(), B.data_ptr(), G.data_ptr(), dA.data_ptr(), dB.data_ptr(),
                            M, N, K, sp))
+
+        def e2e_call(i, ins):
+            c = kaio.matmul_tc(ins[0], ins[1], out=C, stream=stream, out_dtype=out_t)
+            return [c, *kaio.matmul_tc_backward(ins[0], ins[1], ins[2], stream=stream, out_dtype=out_t)]
+        e2e_case = ([A, B, G], e2e_call, {})
 
         wbytes = 0
         units_bytes = 0
@@ -424,34 +443,44 @@ def run_kaio(args, cfg_name, ws, rank, local, dist):
     t_max_ms = max_over_ranks(dist, t_ms, device)
     per_step_s = t_max_ms / 1e3 / steps
 
-    # End to end through the public API: per step, copy x in from pinned host
-    # memory, run the projection, read the three outputs back.
+    # End to end through the public API: per step, copy the step's inputs in
+    # from pinned host memory, make the call(s), read every result back.
     e2e = None
-    if kind == "qkv" and not args.no_e2e:
-        hx = torch.from_numpy(inp.x.copy()).pin_memory()
-        ho = [torch.empty((M, N), dtype=torch.float16).pin_memory() for _ in range(3)]
-        xin = torch.empty_like(x)
-        e_steps = min(args.steps, 2000)
+    if not args.no_e2e:
+        dev_in, call, extra = e2e_case
+        h_in = [t.cpu().pin_memory() for t in dev_in]
+        d_in = [torch.empty_like(t) for t in dev_in]
+        h_out = None
+        e_steps = min(args.steps, 2000 if kind in ("qkv", "qkv8") else 100)
+        h2d = sum(t.numel() * t.element_size() for t in h_in)
+
+        def e2e_step(i):
+            nonlocal h_out
+            for d, h in zip(d_in, h_in):
+                d.copy_(h, non_blocking=True)
+            res = call(i, d_in)
+            if h_out is None:
+                h_out = [torch.empty(r.shape, dtype=r.dtype).pin_memory() for r in res]
+            for h, r in zip(h_out, res):
+                h.copy_(r, non_blocking=True)
+
         with torch.cuda.stream(stream):
             for i in range(3):
-                xin.copy_(hx, non_blocking=True)
-                kaio.qkv_project_int4(xin, *sets[i % len(sets)], out=outs, stream=stream)
-                for o, h in zip(outs, ho):
-                    h.copy_(o, non_blocking=True)
+                e2e_step(i)
             stream.synchronize()
             barrier(dist)
             t0 = time.perf_counter()
             for i in range(e_steps):
-                xin.copy_(hx, non_blocking=True)
-                kaio.qkv_project_int4(xin, *sets[i % len(sets)], out=outs, stream=stream)
-                for o, h in zip(outs, ho):
-                    h.copy_(o, non_blocking=True)
+                e2e_step(i)
             stream.synchronize()
             t1 = time.perf_counter()
         te = max_over_ranks(dist, t1 - t0, device)
-        e2e = {"value": round(ws * units_bytes * e_steps / te / 1e9, 3), "unit": "GB/s",
-               "h2d_bytes_per_step": M * K * 2, "d2h_bytes_per_step": 3 * M * N * 2,
-               "steps": e_steps, "weights_resident": True}
+        d2h = sum(t.numel() * t.element_size() for t in h_out)
+        if kind in ("matmul", "matmul16"):
+            e2e = {"value": round(ws * flops * e_steps / te / 1e12, 3), "unit": "TFLOP/s"}
+        else:
+            e2e = {"value": round(ws * units_bytes * e_steps / te / 1e9, 3), "unit": "GB/s"}
+        e2e.update({"h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e_steps, **extra})
 
     if rank != 0:
         return None
@@ -510,71 +539,75 @@ def run_kaio(args, cfg_name, ws, rank, local, dist):
         "gpu_launches": steps * launches_per_step,
         "clocks": clk.summary(),
     }
-    if not args.no_cpu_baseline and ws == 1 and kind != "matmul" and kind != "matmul16":
+    if not args.no_cpu_baseline and ws == 1:
         line["cpu_baseline"] = cpu_baseline(cfg_name, budget_s=args.cpu_budget)
     return line
 
 
 # ---------------------------------------------------------------- oracle arm
-def oracle_step_fn(cfg_name, frac):
-    """One oracle evaluation on a column sample (fraction `frac` of N)."""
+def oracle_sample(cfg_name, frac):
+    """One oracle evaluation of workload `cfg_name` on a sample of fraction
+    `frac`; returns (step, amount, n, extent, noun, unit) where `amount` is the
+    work one step does in the metric's unit (bytes for GB/s, FLOPs for
+    TFLOP/s) and n of extent `noun`s were sampled."""
     import numpy as np
 
     import oracle
-    from qkv_projection_gb300.inputs import qkv_inputs
 
     kind, M, N, K = CONFIGS[cfg_name]
     if kind in DEQUANT_TYPES:
-        return dequant_oracle_step_fn(cfg_name, frac)
+        from oracle import dequant_group as dg
+        from qkv_projection_gb300.inputs import dequant_group_inputs
+        fdt, qdt = DEQUANT_TYPES[kind]
+        rows = max(1, int(round(M * frac)))
+        dy, q, sc = dequant_group_inputs(rows, N, K, fdt, seed=0, q_dtype=qdt)
+
+        def step():
+            if kind == "dqbwd":
+                dg.dequantize_per_group_backward_ref(dy, sc, K, fdt)
+            else:
+                dg.dequantize_per_group_ref(q, sc, K, fdt)
+        return step, dequant_bytes(kind, rows, N, K), rows, M, "rows", "GB/s"
+    if kind in ("matmul", "matmul16"):
+        from qkv_projection_gb300.inputs import dense_inputs
+        a, b, g = dense_inputs(M, N, K, seed=0)
+        r = max(1, int(round(M * frac)))
+        c = max(1, int(round(N * frac)))
+        rows, cols = np.arange(r), np.arange(c)
+
+        def step():
+            oracle.matmul_rows(a, b, rows)                        # rows of C = A B
+            oracle.matmul_rows(g, np.ascontiguousarray(b.T), rows)  # rows of dA = G B^T
+            oracle.matmul_ref(np.ascontiguousarray(a.T), np.ascontiguousarray(g[:, cols]))  # columns of dB = A^T G
+        return step, 2 * r * K * N + 2 * r * N * K + 2 * M * K * c, r, M, "rows (and columns of dB)", "TFLOP/s"
+    ncols = max(8, int(round(N * frac)) // 8 * 8)
     if kind == "qkv8":
         from qkv_projection_gb300.inputs import qkv_int8_inputs
         inp8 = qkv_int8_inputs(M, N, K, seed=0)
-        ncols = max(8, int(round(N * frac)) // 8 * 8)
         ws8 = [np.ascontiguousarray(w[:, :ncols]) for w in inp8.weights()]
 
-        def step8():
+        def step():
             oracle.qkv_project_int8_ref(inp8.x, *ws8, *inp8.scales())
-        return step8, qkv8_bytes(M, ncols, K)[0], ncols
+        return step, qkv8_bytes(M, ncols, K)[0], ncols, N, "columns", "GB/s"
+    from qkv_projection_gb300.inputs import qkv_inputs
     inp = qkv_inputs(M, N, K, seed=0)
-    ncols = max(8, int(round(N * frac)) // 8 * 8)
-    cols = np.arange(ncols)
-    sub = [inp.x] + [np.ascontiguousarray(w[:, cols]) for w in inp.weights()] + \
-          [np.ascontiguousarray(s[:, cols]) for s in inp.scales()]
-    wbytes = qkv_bytes(M, ncols, K)[0]
+    sub = [inp.x] + [np.ascontiguousarray(w[:, :ncols]) for w in inp.weights()] + \
+          [np.ascontiguousarray(s_[:, :ncols]) for s_ in inp.scales()]
 
     def step():
         oracle.qkv_project_int4_ref(*sub)
-    return step, wbytes, ncols
+    return step, qkv_bytes(M, ncols, K)[0], ncols, N, "columns", "GB/s"
 
 
-def dequant_oracle_step_fn(cfg_name, frac):
-    """One oracle evaluation of a per-group dequantisation on a row sample
-    (fraction `frac` of the outer rows); returns (step, bytes, rows)."""
-    from oracle import dequant_group as dg
-    from qkv_projection_gb300.inputs import dequant_group_inputs
-
-    kind, outer, axis, group = CONFIGS[cfg_name]
-    fdt, qdt = DEQUANT_TYPES[kind]
-    rows = max(1, int(round(outer * frac)))
-    dy, q, sc = dequant_group_inputs(rows, axis, group, fdt, seed=0, q_dtype=qdt)
-    nbytes = dequant_bytes(kind, rows, axis, group)
-
-    def step():
-        if kind == "dqbwd":
-            dg.dequantize_per_group_backward_ref(dy, sc, group, fdt)
-        else:
-            dg.dequantize_per_group_ref(q, sc, group, fdt)
-    return step, nbytes, rows
+def _per_unit(amount, unit):
+    return amount / (1e12 if unit == "TFLOP/s" else 1e9)
 
 
 def cpu_baseline(cfg_name, budget_s=15.0):
     kind, M, N, K = CONFIGS[cfg_name]
-    if kind in DEQUANT_TYPES:
-        step, wb, nrows = dequant_oracle_step_fn(cfg_name, 1.0 / 64)
-        what = f"{nrows} of {M} rows"
-    else:
-        step, wb, ncols = oracle_step_fn(cfg_name, 1.0 if N * K <= 4096 * 4096 else 0.125)
-        what = f"{ncols} of {N} columns"
+    frac = (1.0 / 64 if kind in DEQUANT_TYPES else 1.0 / 32 if kind in ("matmul", "matmul16")
+            else 1.0 if N * K <= 4096 * 4096 else 0.125)
+    step, amount, n, extent, noun, unit = oracle_sample(cfg_name, frac)
     t0 = time.perf_counter()
     step()
     one = time.perf_counter() - t0
@@ -583,9 +616,9 @@ def cpu_baseline(cfg_name, budget_s=15.0):
     for _ in range(reps):
         step()
     dt = time.perf_counter() - t0
-    return {"value": round(wb * reps / dt / 1e9, 4), "unit": "GB/s", "cores": os.cpu_count(),
+    return {"value": round(_per_unit(amount, unit) * reps / dt, 5), "unit": unit, "cores": os.cpu_count(),
             "kind": "oracle",
-            "sample": f"{reps} oracle evaluations of {cfg_name} on {what} "
+            "sample": f"{reps} oracle evaluations of {cfg_name} on {n} of {extent} {noun} "
                       f"(numpy float64; BLAS may use up to {os.cpu_count()} threads)"}
 
 
@@ -593,37 +626,31 @@ def run_reference(args, cfg_name, ws, rank):
     kind, M, N, K = CONFIGS[cfg_name]
     if rank != 0:
         return None
-    if kind in ("matmul", "matmul16"):
-        return {"impl": "reference", "unavailable": "the oracle arm covers the W4A16 and dequantisation workloads"}
-    # Size each step's sample (columns of W, or rows of a dequantisation) so the
-    # whole run takes about --ref-seconds.
-    dq = kind in DEQUANT_TYPES
-    extent = M if dq else N
+    # Size each step's sample so that the whole run takes about --ref-seconds.
     total_steps = args.steps + max(args.warmup, 3)
-    probe, _, n_probe = oracle_step_fn(cfg_name, 1.0 / 64)
+    probe, _, n_probe, extent, _, _ = oracle_sample(cfg_name, 1.0 / 64)
     t0 = time.perf_counter()
     probe()
     per_unit = (time.perf_counter() - t0) / n_probe
     frac = min(1.0, max(8.0 / extent, args.ref_seconds / total_steps / max(per_unit, 1e-9) / extent))
-    step, wb, ncols = oracle_step_fn(cfg_name, frac)
+    step, amount, n, extent, noun, unit = oracle_sample(cfg_name, frac)
     for _ in range(max(args.warmup, 3)):
         step()
     t0 = time.perf_counter()
     for _ in range(args.steps):
         step()
     dt = time.perf_counter() - t0
-    value = wb * args.steps / dt / 1e9
-    sample = (f"each step: one oracle evaluation of {cfg_name} on {ncols} of {extent} "
-              f"{'rows' if dq else 'columns'} (numpy float64)")
+    value = _per_unit(amount, unit) * args.steps / dt
+    sample = f"each step: one oracle evaluation of {cfg_name} on {n} of {extent} {noun} (numpy float64)"
     return {
-        "impl": "reference", "metric": METRICS[kind], "value": round(value, 5), "unit": "GB/s",
+        "impl": "reference", "metric": METRICS[kind], "value": round(value, 6), "unit": unit,
         "n_gpus": ws, "steps": args.steps, "warmup": max(args.warmup, 3),
         "ms_per_step": round(dt / args.steps * 1e3, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
         "config": {"workload": cfg_name, **config_shape(kind, M, N, K)},
-        "cpu_baseline": {"value": round(value, 5), "unit": "GB/s", "cores": os.cpu_count(),
+        "cpu_baseline": {"value": round(value, 6), "unit": unit, "cores": os.cpu_count(),
                          "kind": "oracle", "sample": sample},
-        "e2e": {"value": round(value, 5), "unit": "GB/s", "h2d_bytes_per_step": 0,
+        "e2e": {"value": round(value, 6), "unit": unit, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
 
