@@ -291,7 +291,7 @@ __global__ void __launch_bounds__(PTHREADS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < PSTAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1 + PDQ_WARPS);  // MMA commit + every dequant warp
+      mbar_init(&empty[s], 1 + PDQ_WARPS);  // every dequant warp + the release after the MMAs
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&a_full[a], PDQ_WARPS);
@@ -354,22 +354,22 @@ __global__ void __launch_bounds__(PTHREADS, 1)
       constexpr uint32_t idesc = idesc_f16_f32(PBN, PBM, false, false);
       int st = 0, a = 0;
       uint32_t aph = 0, cph = 0;
-      bool ahead = false;          // the current A stage was seen full by a look-ahead test
       for (int tile = blockIdx.x; tile < p.tiles; tile += gridDim.x) {
         if (!mbar_wait(&acc_empty, cph ^ 1, abort, &g_tc_err)) break;
         tc_fence_after();
         bool ok = true;
         for (int ks = 0; ks < nks && ok; ++ks) {
           // No wait on the stage itself: an A stage is full only after the
-          // dequant warps have waited for this stage, so it has landed.
+          // dequant warps have waited for this stage, so it has landed. The
+          // MMA thread does nothing but wait for A stages, issue and commit
+          // them: it releases no shared-memory stage (the dequant warps do,
+          // below) and tests no barrier ahead -- each such operation costs
+          // this thread 150-300 cycles between MMAs.
           const uint64_t bd0 = sdesc_sw128(smem_u32(smem + st * PSTAGE_BYTES), 16, 1024);
           const uint32_t blo = static_cast<uint32_t>(bd0), bhi = static_cast<uint32_t>(bd0 >> 32);
           for (int hh = 0; hh < 2; ++hh) {
-            if (!ahead && !mbar_wait(&a_full[a], aph, abort, &g_tc_err)) { ok = false; break; }
+            if (!mbar_wait(&a_full[a], aph, abort, &g_tc_err)) { ok = false; break; }
             tc_fence_after();
-            // Test the next A stage now; the test's latency overlaps this
-            // stage's MMA issue, and a stage already full needs no wait.
-            ahead = mbar_test_wait(&a_full[a ^ 1], a == 1 ? aph ^ 1 : aph);
 #pragma unroll
             for (int q = 0; q < 3; ++q) {
 #pragma unroll
@@ -383,7 +383,6 @@ __global__ void __launch_bounds__(PTHREADS, 1)
             if (++a == 2) { a = 0; aph ^= 1; }
           }
           if (!ok) break;
-          umma_commit(&empty[st]);
           if (++st == PSTAGES) st = 0;
         }
         if (!ok) break;
@@ -403,6 +402,7 @@ __global__ void __launch_bounds__(PTHREADS, 1)
     const int nl = 32 * sp + lane;
     const uint32_t lane_base = static_cast<uint32_t>(32 * sp) << 16;
     int st = 0, a = 0;
+    int rel_st = -1;   // shared-memory stage of the previous k-step, not yet released
     uint32_t ph = 0, aph = 0, cph = 0;
     for (int tile = blockIdx.x; tile < p.tiles; tile += gridDim.x) {
       const int m0 = (tile % p.m_blocks) * PBM, n0 = (tile / p.m_blocks) * PBN;
@@ -425,6 +425,10 @@ __global__ void __launch_bounds__(PTHREADS, 1)
         (void)ss;
         for (int hh = 0; hh < 2; ++hh) {
           if (!mbar_wait(&a_empty[a], aph ^ 1, abort, &g_tc_err)) { ok = false; break; }
+          // A stage 1 is free once the MMAs of the previous k-step's second
+          // half have completed, i.e. every MMA reading that k-step's x tile:
+          // one warp releases its shared-memory stage on the MMA's behalf.
+          if (hh == 1 && rel_st >= 0 && warp == 2 && lane == 0) mbar_arrive(&empty[rel_st]);
           tc_fence_after();
 #pragma unroll
           for (int q = 0; q < 3; ++q) {
@@ -459,6 +463,7 @@ __global__ void __launch_bounds__(PTHREADS, 1)
         if (!ok) break;
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[st]);
+        rel_st = st;
         if (++st == PSTAGES) { st = 0; ph ^= 1; }
       }
       if (!ok) break;
