@@ -12,8 +12,9 @@
 //    projection, applied to the f32 accumulator in the epilogue.
 //
 // Both share one pipeline shape: a TMA producer warp fills a ring of shared
-// memory stages, a single thread issues tcgen05.mma into f32 accumulators in
-// tensor memory, and the remaining warps drain the accumulators with
+// memory stages, MMA-issuing threads (one; in the projection kernel one per
+// projection) issue tcgen05.mma into f32 accumulators in tensor memory, and
+// the remaining warps drain the accumulators with
 // tcgen05.ld and write the outputs. Every wait on an mbarrier is bounded.
 //
 // Dense: A and B both come from shared memory (128B-swizzled TMA tiles);
@@ -246,8 +247,9 @@ constexpr int PBN = 128;                 // output columns per tile (MMA M)
 constexpr int PBK = 64;                  // K per TMA stage
 constexpr int PSTAGES = 4;
 constexpr int PX_BYTES = PBM * PBK * 2;          // 16384
-constexpr int PTHREADS = 320;                    // w0 TMA, w1 MMA, w2..9 dequant + epilogue
+constexpr int PMMA_WARPS = 3;                    // one MMA-issuing warp per projection
 constexpr int PDQ_WARPS = 8;
+constexpr int PTHREADS = (1 + PMMA_WARPS + PDQ_WARPS) * 32;   // w0 TMA, w1..3 MMA, w4..11 dequant + epilogue
 constexpr uint32_t PTMEM_COLS = 512;
 constexpr uint32_t PA_COL0 = 384;                // A stages after the three accumulators
 constexpr uint32_t PA_STAGE_COLS = 48;           // 3 projections x 16 columns (32 K)
@@ -283,7 +285,7 @@ __global__ void __launch_bounds__(PTHREADS, 1)
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = align_smem_1024(smem_raw);
   __shared__ __align__(8) uint64_t full[PSTAGES], empty[PSTAGES], a_full[2], a_empty[2],
-      acc_full, acc_empty, mma_done;
+      acc_full, acc_empty, mma_done[PMMA_WARPS];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
 
@@ -295,11 +297,11 @@ __global__ void __launch_bounds__(PTHREADS, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&a_full[a], PDQ_WARPS);
-      mbar_init(&a_empty[a], 1);
+      mbar_init(&a_empty[a], PMMA_WARPS);   // one commit per MMA warp
     }
-    mbar_init(&acc_full, 1);
+    mbar_init(&acc_full, PMMA_WARPS);
     mbar_init(&acc_empty, PDQ_WARPS);
-    mbar_init(&mma_done, 1);
+    for (int w = 0; w < PMMA_WARPS; ++w) mbar_init(&mma_done[w], 1);
     abort_flag = 0;
     fence_mbar_init();
   }
@@ -349,7 +351,16 @@ __global__ void __launch_bounds__(PTHREADS, 1)
       for (int s2 = 0; s2 < PSTAGES; ++s2)
         if (fills[s2]) mbar_wait_drain(&full[s2], (fills[s2] - 1) & 1, &g_tc_err);
     }
-  } else if (warp == 1) {
+  } else if (warp <= PMMA_WARPS) {
+    // MMA warp q issues projection q's MMAs into its accumulator D[q]; three
+    // issuing warps overlap one another's barrier waits and commits with MMAs.
+    // No wait on the shared-memory stage itself: an A stage is full only after
+    // the dequant warps have waited for the stage, so it has landed. These
+    // warps do nothing but wait for A stages, issue and commit them: they
+    // release no shared-memory stage (the dequant warps do, below) and test no
+    // barrier ahead -- each such operation costs the issuing thread 150-300
+    // cycles between MMAs.
+    const int q = warp - 1;
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_f16_f32(PBN, PBM, false, false);
       int st = 0, a = 0;
@@ -359,25 +370,16 @@ __global__ void __launch_bounds__(PTHREADS, 1)
         tc_fence_after();
         bool ok = true;
         for (int ks = 0; ks < nks && ok; ++ks) {
-          // No wait on the stage itself: an A stage is full only after the
-          // dequant warps have waited for this stage, so it has landed. The
-          // MMA thread does nothing but wait for A stages, issue and commit
-          // them: it releases no shared-memory stage (the dequant warps do,
-          // below) and tests no barrier ahead -- each such operation costs
-          // this thread 150-300 cycles between MMAs.
           const uint64_t bd0 = sdesc_sw128(smem_u32(smem + st * PSTAGE_BYTES), 16, 1024);
           const uint32_t blo = static_cast<uint32_t>(bd0), bhi = static_cast<uint32_t>(bd0 >> 32);
           for (int hh = 0; hh < 2; ++hh) {
             if (!mbar_wait(&a_full[a], aph, abort, &g_tc_err)) { ok = false; break; }
             tc_fence_after();
 #pragma unroll
-            for (int q = 0; q < 3; ++q) {
-#pragma unroll
-              for (int kk = 0; kk < 2; ++kk) {
-                const uint32_t at = tmem + PA_COL0 + a * PA_STAGE_COLS + q * 16 + kk * 8;
-                umma_ts_lohi(tmem + q * PBM, at, blo + (((2 * hh + kk) * 32) >> 4), bhi, idesc,
-                             (ks | hh | kk) != 0 ? 1u : 0u);
-              }
+            for (int kk = 0; kk < 2; ++kk) {
+              const uint32_t at = tmem + PA_COL0 + a * PA_STAGE_COLS + q * 16 + kk * 8;
+              umma_ts_lohi(tmem + q * PBM, at, blo + (((2 * hh + kk) * 32) >> 4), bhi, idesc,
+                           (ks | hh | kk) != 0 ? 1u : 0u);
             }
             umma_commit(&a_empty[a]);
             if (++a == 2) { a = 0; aph ^= 1; }
@@ -389,8 +391,8 @@ __global__ void __launch_bounds__(PTHREADS, 1)
         umma_commit(&acc_full);
         cph ^= 1;
       }
-      umma_commit(&mma_done);
-      mbar_wait_drain(&mma_done, 0, &g_tc_err);
+      umma_commit(&mma_done[q]);
+      mbar_wait_drain(&mma_done[q], 0, &g_tc_err);
     }
   } else {
     // Dequant + epilogue warps. TMEM lane group sp = warp % 4: this thread owns
@@ -398,7 +400,7 @@ __global__ void __launch_bounds__(PTHREADS, 1)
     // 16 K of each 32-K A stage this warp fills (two INT4 or four INT8 packed
     // rows), and the half of the x rows it drains in the epilogue.
     const int sp = warp & 3;
-    const int hf = (warp - 2) >> 2;
+    const int hf = (warp - 1 - PMMA_WARPS) >> 2;
     const int nl = 32 * sp + lane;
     const uint32_t lane_base = static_cast<uint32_t>(32 * sp) << 16;
     int st = 0, a = 0;
@@ -428,7 +430,7 @@ __global__ void __launch_bounds__(PTHREADS, 1)
           // A stage 1 is free once the MMAs of the previous k-step's second
           // half have completed, i.e. every MMA reading that k-step's x tile:
           // one warp releases its shared-memory stage on the MMA's behalf.
-          if (hh == 1 && rel_st >= 0 && warp == 2 && lane == 0) mbar_arrive(&empty[rel_st]);
+          if (hh == 1 && rel_st >= 0 && warp == 1 + PMMA_WARPS && lane == 0) mbar_arrive(&empty[rel_st]);
           tc_fence_after();
 #pragma unroll
           for (int q = 0; q < 3; ++q) {
