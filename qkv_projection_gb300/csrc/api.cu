@@ -187,6 +187,29 @@ int zero_outputs(const Span* out, int n, cudaStream_t stream) {
     if (st__ != KAIO_OK) return st__; \
   } while (0)
 
+// The checks every projection entry makes after its own null-pointer and
+// dimension rules, in this order: 16-byte alignment, size limits (packed
+// words of one weight tensor, M x K), overlap, the current device, the empty
+// problem (M == 0 or N == 0: nothing to do), output residency, K == 0 (the
+// outputs are the empty sum: zeroed here), input residency. *run is set when
+// the caller must launch a kernel; *dev and *info then describe the device.
+int check_projection(const Span* in, int n_in, const Span* out, uint64_t packed_words, uint32_t M,
+                     uint32_t N, uint32_t K, cudaStream_t stream, bool* run, int* dev, DeviceInfo* info) {
+  *run = false;
+  KAIO_TRY(check_aligned(in, n_in));
+  KAIO_TRY(check_aligned(out, 3));
+  if (packed_words > 0x7FFFFFFFull || static_cast<uint64_t>(M) * K > (1ull << 40))
+    return fail(KAIO_ERR_INVALID_VALUE, "problem too large (M=%u N=%u K=%u)", M, N, K);
+  KAIO_TRY(check_overlap(in, n_in, out, 3));
+  KAIO_TRY(current_device(dev, info));
+  if (M == 0 || N == 0) return KAIO_OK;
+  KAIO_TRY(check_on_device(out, 3, *dev));
+  if (K == 0) return zero_outputs(out, 3, stream);
+  KAIO_TRY(check_on_device(in, n_in, *dev));
+  *run = true;
+  return KAIO_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -224,18 +247,11 @@ int kaio_qkv_project_int4(const void* x, const uint32_t* wq, const uint32_t* wk,
     return fail(KAIO_ERR_INVALID_VALUE, "K (%u) must be a multiple of group_size (128)", K);
   if (N % 8 != 0)
     return fail(KAIO_ERR_INVALID_VALUE, "N (%u) must be a multiple of 8 (16-byte rows)", N);
-  KAIO_TRY(check_aligned(in, 7));
-  KAIO_TRY(check_aligned(out, 3));
-  if (static_cast<uint64_t>(K) / 8 * N > 0x7FFFFFFFull || static_cast<uint64_t>(M) * K > (1ull << 40))
-    return fail(KAIO_ERR_INVALID_VALUE, "problem too large (M=%u N=%u K=%u)", M, N, K);
-  KAIO_TRY(check_overlap(in, 7, out, 3));
+  bool run;
   int dev;
   DeviceInfo info;
-  KAIO_TRY(current_device(&dev, &info));
-  if (M == 0 || N == 0) return KAIO_OK;
-  KAIO_TRY(check_on_device(out, 3, dev));
-  if (K == 0) return zero_outputs(out, 3, stream);
-  KAIO_TRY(check_on_device(in, 7, dev));
+  KAIO_TRY(check_projection(in, 7, out, static_cast<uint64_t>(K) / 8 * N, M, N, K, stream, &run, &dev, &info));
+  if (!run) return KAIO_OK;
 
   const uint32_t* w3[3] = {wq, wk, wv};
   const __half* s3[3] = {static_cast<const __half*>(sq), static_cast<const __half*>(sk),
@@ -318,18 +334,11 @@ int kaio_qkv_project_int8(const void* x, const uint32_t* wq, const uint32_t* wk,
     return fail(KAIO_ERR_INVALID_VALUE, "K (%u) must be a multiple of 128 (the kernels' K group)", K);
   if (N % 8 != 0)
     return fail(KAIO_ERR_INVALID_VALUE, "N (%u) must be a multiple of 8 (16-byte rows)", N);
-  KAIO_TRY(check_aligned(in, 4));
-  KAIO_TRY(check_aligned(out, 3));
-  if (static_cast<uint64_t>(K) / 4 * N > 0x7FFFFFFFull || static_cast<uint64_t>(M) * K > (1ull << 40))
-    return fail(KAIO_ERR_INVALID_VALUE, "problem too large (M=%u N=%u K=%u)", M, N, K);
-  KAIO_TRY(check_overlap(in, 4, out, 3));
+  bool run;
   int dev;
   DeviceInfo info;
-  KAIO_TRY(current_device(&dev, &info));
-  if (M == 0 || N == 0) return KAIO_OK;
-  KAIO_TRY(check_on_device(out, 3, dev));
-  if (K == 0) return zero_outputs(out, 3, stream);
-  KAIO_TRY(check_on_device(in, 4, dev));
+  KAIO_TRY(check_projection(in, 4, out, static_cast<uint64_t>(K) / 4 * N, M, N, K, stream, &run, &dev, &info));
+  if (!run) return KAIO_OK;
 
   const uint32_t* w3[3] = {wq, wk, wv};
   const float sc3[3] = {scale_q, scale_k, scale_v};
@@ -377,18 +386,11 @@ int kaio_qkv_project_int4_noalloc(const void* x, const uint32_t* wq, const uint3
     return fail(KAIO_ERR_INVALID_VALUE,
                 "N (%u) exceeds the allocation-free limit (%d column groups of 256 in its "
                 "fixed %zu-byte scratch)", N, kaio::noalloc_max_counters(), kaio::kNoAllocScratchBytes);
-  KAIO_TRY(check_aligned(in, 7));
-  KAIO_TRY(check_aligned(out, 3));
-  if (static_cast<uint64_t>(K) / 8 * N > 0x7FFFFFFFull)
-    return fail(KAIO_ERR_INVALID_VALUE, "problem too large (M=%u N=%u K=%u)", M, N, K);
-  KAIO_TRY(check_overlap(in, 7, out, 3));
+  bool run;
   int dev;
   DeviceInfo info;
-  KAIO_TRY(current_device(&dev, &info));
-  if (M == 0 || N == 0) return KAIO_OK;
-  KAIO_TRY(check_on_device(out, 3, dev));
-  if (K == 0) return zero_outputs(out, 3, stream);
-  KAIO_TRY(check_on_device(in, 7, dev));
+  KAIO_TRY(check_projection(in, 7, out, static_cast<uint64_t>(K) / 8 * N, M, N, K, stream, &run, &dev, &info));
+  if (!run) return KAIO_OK;
   kaio::DecodeParams prm{};
   prm.x = static_cast<const __half*>(x);
   const uint32_t* w3[3] = {wq, wk, wv};
