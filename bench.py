@@ -1,10 +1,16 @@
 """Benchmark of the W4A16 fused QKV projection (and the dense tensor-core matmul).
 
 One step = one pass of the hot path over one batch: one kaio_qkv_project_int4
-call (Q, K and V together) on the chosen workload. Default workload: the decode
-projection M=1, K=N=4096 (25.95 MB of packed weights and scales per step).
+call (Q, K and V together) on the chosen workload. Default workload: the
+largest configuration, the prefill projection M = N = K = 4096 (412.3 GFLOP
+per step, tensor-core bound); the decode shapes are selected with --config.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl kaio|reference]
+
+Timing: the K steps are captured in one CUDA graph; that window of K steps is
+replayed back to back for at least --min-seconds, each replay bracketed by CUDA
+events on the launching stream, and the per-step time is that of the median
+window (min and max are reported beside it).
 
 Prints one JSON line (rank 0). Under torchrun (N > 1) every rank runs an
 independent replica on its own GPU (the projection has no exchange step) and
@@ -26,17 +32,17 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 DEFAULT_STEPS = {
-    "qkv_decode_m1_k4096_n4096": 100000,
-    "qkv_m16_k256_n128": 100000,
-    "qkv_batched_decode_m16_k8192_n8192": 40000,
-    "qkv_prefill_m4096_k4096_n4096": 2000,
-    "matmul_f16_m4096_n4096_k4096_fwd_bwd": 1000,
-    "matmul_f16out_m4096_n4096_k4096_fwd_bwd": 1000,
-    "qkv8_decode_m1_k4096_n4096": 50000,
-    "qkv8_batched_decode_m16_k8192_n8192": 20000,
-    "qkv8_prefill_m4096_k4096_n4096": 2000,
-    "dequant_bwd_bf16_outer8192_axis8192_g128": 4000,
-    "dequant_fwd_s8_f16_outer8192_axis8192_g128": 4000,
+    "qkv_decode_m1_k4096_n4096": 200,
+    "qkv_m16_k256_n128": 200,
+    "qkv_batched_decode_m16_k8192_n8192": 100,
+    "qkv_prefill_m4096_k4096_n4096": 20,
+    "matmul_f16_m4096_n4096_k4096_fwd_bwd": 20,
+    "matmul_f16out_m4096_n4096_k4096_fwd_bwd": 20,
+    "qkv8_decode_m1_k4096_n4096": 200,
+    "qkv8_batched_decode_m16_k8192_n8192": 100,
+    "qkv8_prefill_m4096_k4096_n4096": 20,
+    "dequant_bwd_bf16_outer8192_axis8192_g128": 50,
+    "dequant_fwd_s8_f16_outer8192_axis8192_g128": 50,
 }
 CONFIGS = {
     # name: (kind, M, N, K)
@@ -57,7 +63,7 @@ CONFIGS = {
 }
 # element types of the per-group dequantisation workloads: (float type, quantised type)
 DEQUANT_TYPES = {"dqbwd": ("bf16", "s8"), "dqfwd": ("f16", "s8")}
-DEFAULT_CONFIG = "qkv_decode_m1_k4096_n4096"
+DEFAULT_CONFIG = "qkv_prefill_m4096_k4096_n4096"
 METRIC = "W4A16 QKV TFLOP/s and weight GB/s (1xGB300) as % of roofline"
 METRICS = {
     "qkv": METRIC,
@@ -291,11 +297,7 @@ def run_kaio(args, cfg_name, ws, rank, local, dist):
         units_bytes = wbytes
         alg_bytes = wbytes + obytes
         flops = qkv_flops(M, N, K)
-        if kaio.qkv_path(M) == 0:
-            split = os.environ.get("KAIO_DECODE_SPLIT", "")
-            kernel_file = {"mma": "decode_cluster.cu", "streamk": "decode_w4a16.cu"}.get(split, "tc_decode.cu")
-        else:
-            kernel_file = "tc_kernels.cu"
+        kernel_file = "tc_decode.cu" if kaio.qkv_path(M) == 0 else "tc_kernels.cu"
         bound = "hbm" if M <= 16 else "tensor"
         launches_per_step = 1
     elif kind == "qkv8":
@@ -401,47 +403,73 @@ def run_kaio(args, cfg_name, ws, rank, local, dist):
         bound = "tensor"
         launches_per_step = 3
 
-    # Warm-up (also allocates the decode workspace outside capture).
+    # Warm-up.
     with torch.cuda.stream(stream):
         for i in range(max(args.warmup, 3)):
             step(i)
     stream.synchronize()
 
-    # Capture up to `chunk` steps in one CUDA graph; replay it to cover K steps.
-    chunk = min(args.steps, 1000 if kind in ("qkv", "qkv8") else 8)
+    # Host cost of one C-ABI call (validation, residency checks, tensor maps,
+    # launch): a host loop of calls with no synchronisation in between.
+    host_us = None
+    if kind in ("qkv", "qkv8"):
+        n_host = 200
+        with torch.cuda.stream(stream):
+            h0 = time.perf_counter()
+            for i in range(n_host):
+                step(i)
+            h1 = time.perf_counter()
+        stream.synchronize()
+        host_us = round((h1 - h0) / n_host * 1e6, 2)
+
+    # One window = the K timed steps, captured in one CUDA graph.
+    steps = args.steps
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.stream(stream):
         with torch.cuda.graph(graph, stream=stream):
-            for i in range(chunk):
+            for i in range(steps):
                 step(i)
     stream.synchronize()
-    replays = -(-args.steps // chunk)
-    steps = replays * chunk
     with torch.cuda.stream(stream):
         for _ in range(2):
             graph.replay()
     stream.synchronize()
 
+    # Replay the window back to back for at least --min-seconds (and at least
+    # 5 times), each replay bracketed by events on the launching stream.
+    probe0 = torch.cuda.Event(enable_timing=True)
+    probe1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        probe0.record(stream)
+        graph.replay()
+        probe1.record(stream)
+    probe1.synchronize()
+    one_ms = max(probe0.elapsed_time(probe1), 1e-3)
+    windows = int(min(20000, max(5, args.min_seconds * 1e3 / one_ms)))
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(windows + 1)]
+
     barrier(dist)
     torch.cuda.synchronize()
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
         time.sleep(0.3)
         w0 = time.perf_counter()
         with torch.cuda.stream(stream):      # replay() launches on the current stream
-            ev0.record(stream)
-            for _ in range(replays):
+            evs[0].record(stream)
+            for r in range(windows):
                 graph.replay()
-            ev1.record(stream)
-        ev1.synchronize()
+                evs[r + 1].record(stream)
+        evs[-1].synchronize()
         clk.mark(w0, time.perf_counter() + 0.05)
         time.sleep(0.1)
     torch.cuda.synchronize()
     barrier(dist)
-    t_ms = ev0.elapsed_time(ev1)
+    win_ms = sorted(evs[r].elapsed_time(evs[r + 1]) for r in range(windows))
+    t_ms = win_ms[len(win_ms) // 2]
     t_max_ms = max_over_ranks(dist, t_ms, device)
     per_step_s = t_max_ms / 1e3 / steps
+    window_stats = {"windows": windows, "steps_per_window": steps,
+                    "ms_per_step_min": round(win_ms[0] / steps, 6),
+                    "ms_per_step_max": round(win_ms[-1] / steps, 6)}
 
     # End to end through the public API: per step, copy the step's inputs in
     # from pinned host memory, make the call(s), read every result back.
@@ -451,7 +479,7 @@ def run_kaio(args, cfg_name, ws, rank, local, dist):
         h_in = [t.cpu().pin_memory() for t in dev_in]
         d_in = [torch.empty_like(t) for t in dev_in]
         h_out = None
-        e_steps = min(args.steps, 2000 if kind in ("qkv", "qkv8") else 100)
+        e_steps = max(args.steps, 200 if M <= 16 and kind in ("qkv", "qkv8") else 20)
         h2d = sum(t.numel() * t.element_size() for t in h_in)
 
         def e2e_step(i):
@@ -476,7 +504,7 @@ def run_kaio(args, cfg_name, ws, rank, local, dist):
             t1 = time.perf_counter()
         te = max_over_ranks(dist, t1 - t0, device)
         d2h = sum(t.numel() * t.element_size() for t in h_out)
-        if kind in ("matmul", "matmul16"):
+        if kind in ("matmul", "matmul16") or bound == "tensor":
             e2e = {"value": round(ws * flops * e_steps / te / 1e12, 3), "unit": "TFLOP/s"}
         else:
             e2e = {"value": round(ws * units_bytes * e_steps / te / 1e9, 3), "unit": "GB/s"}
@@ -497,7 +525,7 @@ def run_kaio(args, cfg_name, ws, rank, local, dist):
                 "frac": round(achieved / tc_peak, 4), "peak_source": peak_src + " bf16 burst (f16 = bf16 rate)"}
     roof["traffic"] = profile_traffic(kernel_file, cfg_name)
 
-    if kind in ("qkv", "qkv8"):
+    if kind in ("qkv", "qkv8") and bound == "hbm":
         value = ws * wbytes / per_step_s / 1e9
         unit = "GB/s"
     elif kind in DEQUANT_TYPES:
@@ -536,7 +564,10 @@ def run_kaio(args, cfg_name, ws, rank, local, dist):
         "weight_gbs": round(ws * wbytes / per_step_s / 1e9, 3) if kind in ("qkv", "qkv8") else None,
         "roofline": roof,
         "e2e": e2e,
-        "gpu_launches": steps * launches_per_step,
+        "gpu_launches": windows * steps * launches_per_step,
+        "timing": {**window_stats, "gpu_launches_per_window": steps * launches_per_step,
+                   "note": "ms_per_step is the median window's; gpu_launches counts every window timed"},
+        "host_us_per_call": host_us,
         "clocks": clk.summary(),
     }
     if not args.no_cpu_baseline and ws == 1:
@@ -580,6 +611,25 @@ def oracle_sample(cfg_name, frac):
             oracle.matmul_rows(g, np.ascontiguousarray(b.T), rows)  # rows of dA = G B^T
             oracle.matmul_ref(np.ascontiguousarray(a.T), np.ascontiguousarray(g[:, cols]))  # columns of dB = A^T G
         return step, 2 * r * K * N + 2 * r * N * K + 2 * M * K * c, r, M, "rows (and columns of dB)", "TFLOP/s"
+    if M > 16:
+        # Tensor-bound shapes: a seeded sample of output rows (always rows 0, 1,
+        # 127, 128 and M-1), in FLOPs of the rows computed.
+        r = max(5, int(round(M * frac)))
+        rows = np.unique(np.concatenate([
+            np.random.default_rng(0).choice(M, r, replace=False), [0, 1, 127, 128, M - 1]]))
+        if kind == "qkv8":
+            from qkv_projection_gb300.inputs import qkv_int8_inputs
+            inp8 = qkv_int8_inputs(M, N, K, seed=0)
+
+            def step():
+                oracle.qkv_project_int8_rows(*inp8.args(), rows)
+        else:
+            from qkv_projection_gb300.inputs import qkv_inputs
+            inp = qkv_inputs(M, N, K, seed=0)
+
+            def step():
+                oracle.qkv_project_int4_rows(*inp.__dict__.values(), rows)
+        return step, qkv_flops(len(rows), N, K), len(rows), M, "rows", "TFLOP/s"
     ncols = max(8, int(round(N * frac)) // 8 * 8)
     if kind == "qkv8":
         from qkv_projection_gb300.inputs import qkv_int8_inputs
@@ -606,7 +656,7 @@ def _per_unit(amount, unit):
 def cpu_baseline(cfg_name, budget_s=15.0):
     kind, M, N, K = CONFIGS[cfg_name]
     frac = (1.0 / 64 if kind in DEQUANT_TYPES else 1.0 / 32 if kind in ("matmul", "matmul16")
-            else 1.0 if N * K <= 4096 * 4096 else 0.125)
+            else 1.0 / 64 if M > 16 else 1.0 if N * K <= 4096 * 4096 else 0.125)
     step, amount, n, extent, noun, unit = oracle_sample(cfg_name, frac)
     t0 = time.perf_counter()
     step()
@@ -665,6 +715,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--min-seconds", type=float, default=2.0,
+                    help="replay the K-step window for at least this long (median window reported)")
     ap.add_argument("--ref-seconds", type=float, default=60.0,
                     help="approximate length of the --impl reference run")
     args = ap.parse_args()

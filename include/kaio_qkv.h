@@ -70,10 +70,9 @@ typedef enum {
  * an output overlapping an input or another output; a pointer not on the
  * current device; misaligned pointer (KAIO_ERR_MISALIGNED).
  *
- * Path: M <= 16 runs the weight-streaming decode kernel (split over K across
- * all SMs; it uses a per-(device, stream) workspace that the library
- * allocates on the first such call and keeps: make that first call outside
- * CUDA-graph capture). M >= 17 runs the tcgen05 tensor-core kernel.
+ * Path: M <= 16 runs the tcgen05 decode kernel (K split across the CTAs of a
+ * thread-block cluster, partial sums reduced in distributed shared memory);
+ * M >= 17 runs the tcgen05 tile kernel. Neither allocates device memory.
  */
 int kaio_qkv_project_int4(const void* x, const uint32_t* wq, const uint32_t* wk,
                           const uint32_t* wv, const void* sq, const void* sk, const void* sv,
@@ -91,8 +90,10 @@ int kaio_qkv_project_int4(const void* x, const uint32_t* wq, const uint32_t* wk,
  *
  * Same arguments, layouts, results and errors as kaio_qkv_project_int4, with
  * these differences:
- *   - M must be <= 16 (it runs the weight-streaming decode kernel); larger M
- *     is rejected with KAIO_ERR_INVALID_VALUE.
+ *   - M must be <= 16 (it runs a stream-K decode kernel that spreads the
+ *     weight stream evenly over every SM and finishes split column groups
+ *     through a global-memory scratch); larger M is rejected with
+ *     KAIO_ERR_INVALID_VALUE.
  *   - The kernel's split-K scratch (group counters and partial sums) lives in
  *     one fixed 8 MiB array inside the library; every GPU that loads the
  *     library holds it until the process exits. N is limited to 3*ceil(N/256)
@@ -104,7 +105,11 @@ int kaio_qkv_project_int4(const void* x, const uint32_t* wq, const uint32_t* wk,
  *     clears the counters it needs (cudaMemsetAsync on `stream`) before its
  *     kernel.
  *   - The first call on each device looks up the array's device address
- *     (cudaGetSymbolAddress); make that first call before any stream capture.
+ *     (cudaGetSymbolAddress) and keeps it for the life of the process; make
+ *     that first call before any stream capture. A device reset
+ *     (cudaDeviceReset, or anything else that destroys the device's primary
+ *     context) is not supported: do not call this entry point again in a
+ *     process after one.
  *   - It calls no cudaMalloc, cudaFree or other allocating routine.
  */
 int kaio_qkv_project_int4_noalloc(const void* x, const uint32_t* wq, const uint32_t* wk,

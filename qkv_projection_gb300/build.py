@@ -17,8 +17,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(HERE, "libkaio_qkv.so")
-SOURCES = ["api.cu", "decode_w4a16.cu", "decode_cluster.cu", "tc_decode.cu", "tc_kernels.cu",
-           "dequant_group.cu"]
+SOURCES = ["api.cu", "decode_w4a16.cu", "tc_decode.cu", "tc_kernels.cu", "dequant_group.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "-I", os.path.join(ROOT, "include")]

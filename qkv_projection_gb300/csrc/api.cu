@@ -1,5 +1,5 @@
-// C ABI of libkaio_qkv: argument validation, device checks, workspace for the
-// split-K decode path, and dispatch to the kernels. No computation happens on
+// C ABI of libkaio_qkv: argument validation, device checks and dispatch to
+// the kernels. No computation happens on
 // the host: every output element is produced by a kernel on the device.
 //
 // The validation mirrors the input contract of the direct-call bridge on
@@ -132,47 +132,6 @@ int check_on_device(const Span* s, int n, int dev) {
   return KAIO_OK;
 }
 
-// ------------------------------------------------- decode split-K workspace
-struct Workspace {
-  void* ptr = nullptr;
-  size_t counter_cap = 0;   // number of u32 counters at the front (kept zero)
-  size_t partial_cap = 0;   // floats after the counters
-};
-std::map<std::pair<int, cudaStream_t>, Workspace> g_ws;
-
-size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
-
-int get_workspace(int dev, cudaStream_t stream, size_t counters, size_t partial_floats,
-                  unsigned** counters_out, float** partials_out) {
-  std::lock_guard<std::mutex> lk(g_mu);
-  Workspace& w = g_ws[{dev, stream}];
-  if (w.ptr == nullptr || counters > w.counter_cap || partial_floats > w.partial_cap) {
-    const size_t ccap = std::max(counters, w.counter_cap);
-    const size_t pcap = std::max(partial_floats, w.partial_cap);
-    if (w.ptr) {
-      // Earlier launches on this stream may still use the old buffer.
-      cudaError_t e = cudaStreamSynchronize(stream);
-      if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize (workspace growth)");
-      cudaFree(w.ptr);
-      w.ptr = nullptr;
-    }
-    const size_t cbytes = align_up(ccap * sizeof(unsigned), 256);
-    cudaError_t e = cudaMalloc(&w.ptr, cbytes + pcap * sizeof(float));
-    if (e != cudaSuccess) {
-      w = Workspace{};
-      return cuda_fail(e, "cudaMalloc (decode workspace)");
-    }
-    e = cudaMemsetAsync(w.ptr, 0, cbytes, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync (decode counters)");
-    w.counter_cap = ccap;
-    w.partial_cap = pcap;
-  }
-  *counters_out = static_cast<unsigned*>(w.ptr);
-  *partials_out = reinterpret_cast<float*>(static_cast<char*>(w.ptr) +
-                                           align_up(w.counter_cap * sizeof(unsigned), 256));
-  return KAIO_OK;
-}
-
 int zero_outputs(const Span* out, int n, cudaStream_t stream) {
   for (int i = 0; i < n; ++i) {
     cudaError_t e = cudaMemsetAsync(const_cast<void*>(out[i].p), 0, out[i].bytes, stream);
@@ -260,60 +219,20 @@ int kaio_qkv_project_int4(const void* x, const uint32_t* wq, const uint32_t* wk,
 
   cudaError_t e;
   if (kaio_qkv_path(M) == 0) {
-    const kaio::DecodePlan pl = kaio::plan_decode(static_cast<int>(M), static_cast<int>(N),
-                                                  static_cast<int>(K), info.sms);
-    // Default: the tcgen05 decode kernel (cluster split-K). KAIO_DECODE_SPLIT
-    // selects one of the three decode kernels instead -- "tc", "mma" (mma.sync,
-    // cluster split-K) or "streamk" (mma.sync, stream-K split with a workspace);
-    // all three compute the same result.
-    const char* force = std::getenv("KAIO_DECODE_SPLIT");
-    const bool want_mma = force && std::strcmp(force, "mma") == 0;
-    const bool want_streamk = force && std::strcmp(force, "streamk") == 0;
-    if (!want_mma && !want_streamk) {
-      const kaio::TcDecodePlan tp = kaio::plan_tc_decode(static_cast<int>(M), static_cast<int>(N),
-                                                         static_cast<int>(K), dev);
-      if (tp.ok) {
-        e = kaio::launch_tc_decode(static_cast<const __half*>(x), w3, s3, o3, static_cast<int>(M),
-                                   static_cast<int>(N), static_cast<int>(K), tp, stream);
-        if (e != cudaSuccess) return cuda_fail(e, "tcgen05 decode kernel launch");
-        return KAIO_OK;
-      }
-    }
-    const kaio::ClusterPlan cp = kaio::plan_decode_cluster(static_cast<int>(M), static_cast<int>(N),
-                                                           static_cast<int>(K), info.sms, dev);
-    if (cp.ok && !want_streamk) {
-      e = kaio::launch_decode_cluster(static_cast<const __half*>(x), w3, s3, o3, static_cast<int>(M),
-                                      static_cast<int>(N), static_cast<int>(K), cp, stream);
-      if (e != cudaSuccess) return cuda_fail(e, "cluster decode kernel launch");
+    const kaio::TcDecodePlan tp = kaio::plan_tc_decode(static_cast<int>(M), static_cast<int>(N),
+                                                       static_cast<int>(K), dev);
+    if (tp.ok) {
+      e = kaio::launch_tc_decode(static_cast<const __half*>(x), w3, s3, o3, static_cast<int>(M),
+                                 static_cast<int>(N), static_cast<int>(K), tp, stream);
+      if (e != cudaSuccess) return cuda_fail(e, "tcgen05 decode kernel launch");
       return KAIO_OK;
     }
-    unsigned* counters = nullptr;
-    float* partials = nullptr;
-    KAIO_TRY(get_workspace(dev, stream, pl.counters, pl.partial_floats, &counters, &partials));
-    kaio::DecodeParams prm{};
-    prm.x = static_cast<const __half*>(x);
-    for (int i = 0; i < 3; ++i) {
-      prm.w[i] = w3[i];
-      prm.s[i] = s3[i];
-      prm.out[i] = o3[i];
-    }
-    prm.M = static_cast<int>(M);
-    prm.N = static_cast<int>(N);
-    prm.K = static_cast<int>(K);
-    prm.groups_per_proj = pl.groups_per_proj;
-    prm.nkb = pl.nkb;
-    prm.units = pl.units;
-    prm.ctas = pl.ctas;
-    prm.xmax_kb = pl.xmax_kb;
-    prm.partials = partials;
-    prm.counters = counters;
-    e = kaio::launch_decode(prm, pl, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
-  } else {
-    e = kaio::launch_tc_w4a16(static_cast<const __half*>(x), w3, s3, o3, static_cast<int>(M),
-                              static_cast<int>(N), static_cast<int>(K), info.sms, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "tcgen05 W4A16 kernel launch");
   }
+  // M >= 17, or no cluster shape of the decode kernel can be resident: the
+  // tile kernel (it takes any M; x rows past M are zero-filled by TMA).
+  e = kaio::launch_tc_w4a16(static_cast<const __half*>(x), w3, s3, o3, static_cast<int>(M),
+                            static_cast<int>(N), static_cast<int>(K), info.sms, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "tcgen05 W4A16 kernel launch");
   return KAIO_OK;
 }
 
@@ -615,11 +534,10 @@ int kaio_device_status(void) {
   cudaError_t e = cudaDeviceSynchronize();
   if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
   const unsigned err_tc = kaio::read_and_clear_tc_errors();
-  const unsigned err_dc = kaio::read_and_clear_decode_errors();
   const unsigned err_td = kaio::read_and_clear_tc_decode_errors();
-  if (err_tc == 0xFFFFFFFFu || err_dc == 0xFFFFFFFFu || err_td == 0xFFFFFFFFu)
+  if (err_tc == 0xFFFFFFFFu || err_td == 0xFFFFFFFFu)
     return fail(KAIO_ERR_CUDA, "could not read the device error word");
-  const unsigned err = err_tc | err_dc | err_td;
+  const unsigned err = err_tc | err_td;
   if (err & kaio::kDevErrTimeoutHost)
     return fail(KAIO_ERR_DEVICE_TIMEOUT, "a kernel gave up a bounded wait (device error word 0x%x)", err);
   return KAIO_OK;

@@ -251,22 +251,6 @@ DecodePlan plan_decode(int M, int N, int K, int num_sms) {
   return pl;
 }
 
-cudaError_t launch_decode(const DecodeParams& prm, const DecodePlan& pl, cudaStream_t stream) {
-  cudaError_t e;
-  if (pl.mt == 1) {
-    e = ensure_smem_limit(reinterpret_cast<const void*>(decode_w4a16_kernel<1>),
-                          static_cast<int>(pl.smem));
-    if (e != cudaSuccess) return e;
-    decode_w4a16_kernel<1><<<pl.ctas, kThreads, pl.smem, stream>>>(prm);
-  } else {
-    e = ensure_smem_limit(reinterpret_cast<const void*>(decode_w4a16_kernel<2>),
-                          static_cast<int>(pl.smem));
-    if (e != cudaSuccess) return e;
-    decode_w4a16_kernel<2><<<pl.ctas, kThreads, pl.smem, stream>>>(prm);
-  }
-  return cudaGetLastError();
-}
-
 // ---------------------------------------------------------------------------
 // Allocation-free variant of the decode launch.
 //

@@ -161,16 +161,6 @@ __device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int c
                "r"(c1)
                : "memory");
 }
-// The same box delivered to `dst`'s offset in every CTA of `cta_mask`; each
-// destination's mbarrier at `bar`'s offset receives the byte count.
-__device__ __forceinline__ void tma_load_2d_mc(void* dst, const CUtensorMap* map, uint64_t* bar, int c0,
-                                               int c1, uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
-      "l"(map), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "h"(cta_mask)
-      : "memory");
-}
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar,
                                             int c0, int c1) {
   asm volatile(
@@ -220,7 +210,6 @@ __device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64
       "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
-// Arrive once on `bar` when every tcgen05.mma issued so far by this thread has completed.
 // tcgen05.mma kind::f16, A from TMEM, B descriptor given as two 32-bit halves.
 __device__ __forceinline__ void umma_ts_lohi(uint32_t d, uint32_t a, uint32_t lo, uint32_t hi,
                                              uint32_t idesc, uint32_t accumulate) {
@@ -231,15 +220,7 @@ __device__ __forceinline__ void umma_ts_lohi(uint32_t d, uint32_t a, uint32_t lo
       : "memory");
 }
 
-// Commit that arrives, once the prior MMAs complete, on the mbarrier at
-// `bar`'s offset in every CTA of the cluster named by `cta_mask`.
-__device__ __forceinline__ void umma_commit_mc(uint64_t* bar, uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(smem_u32(bar)),
-      "h"(cta_mask)
-      : "memory");
-}
+// Arrive once on `bar` when every tcgen05.mma issued so far by this thread has completed.
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(

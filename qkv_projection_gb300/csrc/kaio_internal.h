@@ -40,8 +40,8 @@ struct DecodePlan {
   int counters;
 };
 
+// Stream-K mma.sync decode kernel, run only by the allocation-free entry point.
 DecodePlan plan_decode(int M, int N, int K, int num_sms);
-cudaError_t launch_decode(const DecodeParams& prm, const DecodePlan& pl, cudaStream_t stream);
 
 // Allocation-free decode launch: split-K scratch in a fixed device array of
 // kNoAllocScratchBytes (the first 64 KiB hold group counters). `prm` needs only
@@ -49,26 +49,6 @@ cudaError_t launch_decode(const DecodeParams& prm, const DecodePlan& pl, cudaStr
 constexpr size_t kNoAllocScratchBytes = 8u << 20;
 int noalloc_max_counters();
 cudaError_t launch_decode_noalloc(DecodeParams prm, int dev, int num_sms, cudaStream_t stream);
-
-// Cluster split-K decode (no scratch): a column group of 256 outputs per cluster
-// of S CTAs, each CTA one contiguous range of 128-row K groups.
-struct ClusterPlan {
-  bool ok;
-  int mt;
-  int groups_per_proj, groups;  // column groups over the three projections
-  int ng;                       // K / 128
-  int S;                        // cluster size
-  int nst;                      // ring stages (16 KB each)
-  int sbox;                     // scale rows per TMA box
-  int s_off, x_off;             // shared-memory layout
-  size_t smem;
-  long long est_groups;         // K groups streamed by the busiest SM (cost estimate)
-};
-ClusterPlan plan_decode_cluster(int M, int N, int K, int num_sms, int dev);
-cudaError_t launch_decode_cluster(const __half* x, const uint32_t* const w[3],
-                                  const __half* const s[3], __half* const out[3], int M, int N, int K,
-                                  const ClusterPlan& pl, cudaStream_t stream);
-unsigned read_and_clear_decode_errors();
 
 // tcgen05 decode (M <= 16): 128-column tiles over the three projections, split
 // over K across a cluster of S CTAs.

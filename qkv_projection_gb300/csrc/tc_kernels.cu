@@ -56,17 +56,14 @@ constexpr size_t GSMEM = static_cast<size_t>(GSTAGES) * GSTAGE_BYTES + 1024;
 struct GemmParams {
   void* c;              // f32 or f16 [M, N]
   int M, N, K;
-  int m_pairs, pair_tiles;   // pairs of 128-row blocks; (pair, 256-column block) tiles
+  int m_blocks, tiles;  // 128-row blocks; (128-row, 256-column) tiles
 };
 
 // C16: the epilogue rounds the f32 accumulators to f16 (round-to-nearest-even)
 // and stores f16, fusing the cast the page's backward applies afterwards.
 //
-// The two CTAs of a cluster compute vertically adjacent 128 x 256 tiles, which
-// need the same B tile: each loads its own A tile and one half of B, and
-// multicasts that half into both CTAs' shared memory, so B is read from L2
-// once per pair. A stage may be refilled once both CTAs' MMAs have released it
-// (each MMA thread's commit arrives on the stage's empty barrier in both CTAs).
+// Persistent: CTA c takes tiles c, c + grid, ...; tiles are numbered down the
+// rows first, so the CTAs running at one time share few B tiles, which L2 serves.
 template <bool A_MN, bool B_MN, bool C16>
 __global__ void __launch_bounds__(GTHREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -79,12 +76,10 @@ __global__ void __launch_bounds__(GTHREADS, 1)
   __shared__ int abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int crank = static_cast<int>(cluster_ctarank());
-  constexpr uint16_t kPair = 0x3;                // both CTAs of the cluster
   if (threadIdx.x == 0) {
     for (int s = 0; s < GSTAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 2);                   // one MMA commit from each CTA of the pair
+      mbar_init(&empty[s], 1);                   // the MMA thread's commit
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
@@ -99,13 +94,12 @@ __global__ void __launch_bounds__(GTHREADS, 1)
     tmem_relinquish();
   }
   tc_fence_before();
-  __syncwarp();
-  cluster_sync_all();                            // both CTAs' barriers exist before any multicast
+  __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
   const int nk = (p.K + GBK - 1) / GBK;
   volatile int* abort = &abort_flag;
-  const int tstride = static_cast<int>(gridDim.x) / 2;
+  const int tstride = static_cast<int>(gridDim.x);
 
   if (warp == 0) {
     if (lane == 0) {
@@ -114,15 +108,13 @@ __global__ void __launch_bounds__(GTHREADS, 1)
       int st = 0;
       uint32_t ph = 0;
       uint32_t fills[GSTAGES] = {0, 0, 0, 0};
-      for (int t = static_cast<int>(blockIdx.x) / 2; t < p.pair_tiles; t += tstride) {
-        const int m0 = ((t % p.m_pairs) * 2 + crank) * GBM, n0 = (t / p.m_pairs) * GBN;
+      for (int t = static_cast<int>(blockIdx.x); t < p.tiles; t += tstride) {
+        const int m0 = (t % p.m_blocks) * GBM, n0 = (t / p.m_blocks) * GBN;
         for (int kb = 0; kb < nk; ++kb) {
           if (!mbar_wait(&empty[st], ph ^ 1, abort, &g_tc_err)) goto producer_done;
           ++fills[st];
           unsigned char* sa = smem + st * GSTAGE_BYTES;
           unsigned char* sb = sa + GA_BYTES;
-          // A (own rows) + both halves of B (own half loaded here, the other
-          // multicast by the peer)
           mbar_arrive_expect_tx(&full[st], GSTAGE_BYTES);
           if (!A_MN) {
             tma_load_2d(sa, &tmA, &full[st], kb * GBK, m0);
@@ -131,24 +123,18 @@ __global__ void __launch_bounds__(GTHREADS, 1)
             tma_load_2d(sa + 8192, &tmA, &full[st], m0 + 64, kb * GBK);
           }
           if (!B_MN) {
-            tma_load_2d_mc(sb + crank * (GB_BYTES / 2), &tmB, &full[st], kb * GBK, n0 + crank * (GBN / 2), kPair);
+            tma_load_2d(sb, &tmB, &full[st], kb * GBK, n0);
           } else {
 #pragma unroll
-            for (int q = 2 * crank; q < 2 * crank + 2; ++q)
-              tma_load_2d_mc(sb + q * 8192, &tmB, &full[st], n0 + 64 * q, kb * GBK, kPair);
+            for (int q = 0; q < 4; ++q) tma_load_2d(sb + q * 8192, &tmB, &full[st], n0 + 64 * q, kb * GBK);
           }
           if (++st == GSTAGES) { st = 0; ph ^= 1; }
         }
       }
     producer_done:
-      // No copy may still be landing in shared memory, and no commit of the
-      // peer may still arrive on this CTA's barriers, when the CTA exits: wait
-      // for the last fill of every stage to land and to be released by both CTAs.
+      // No copy may still be landing in shared memory when the CTA exits.
       for (int s2 = 0; s2 < GSTAGES; ++s2)
-        if (fills[s2]) {
-          mbar_wait_drain(&full[s2], (fills[s2] - 1) & 1, &g_tc_err);
-          mbar_wait_drain(&empty[s2], (fills[s2] - 1) & 1, &g_tc_err);
-        }
+        if (fills[s2]) mbar_wait_drain(&full[s2], (fills[s2] - 1) & 1, &g_tc_err);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -157,7 +143,7 @@ __global__ void __launch_bounds__(GTHREADS, 1)
       uint32_t ph = 0;
       int buf = 0;
       uint32_t aph = 0;
-      for (int t = static_cast<int>(blockIdx.x) / 2; t < p.pair_tiles; t += tstride) {
+      for (int t = static_cast<int>(blockIdx.x); t < p.tiles; t += tstride) {
         if (!mbar_wait(&acc_empty[buf], aph ^ 1, abort, &g_tc_err)) break;
         tc_fence_after();
         const uint32_t d = tmem + buf * GBN;
@@ -175,7 +161,7 @@ __global__ void __launch_bounds__(GTHREADS, 1)
                                      : sdesc_sw128(sb + kk * 32, 16, 1024);
             umma_ss(d, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
           }
-          umma_commit_mc(&empty[st], kPair);
+          umma_commit(&empty[st]);
           if (++st == GSTAGES) { st = 0; ph ^= 1; }
         }
         if (!ok) break;
@@ -191,8 +177,8 @@ __global__ void __launch_bounds__(GTHREADS, 1)
     const int sp = warp & 3;
     int buf = 0;
     uint32_t aph = 0;
-    for (int t = static_cast<int>(blockIdx.x) / 2; t < p.pair_tiles; t += tstride) {
-      const int m0 = ((t % p.m_pairs) * 2 + crank) * GBM, n0 = (t / p.m_pairs) * GBN;
+    for (int t = static_cast<int>(blockIdx.x); t < p.tiles; t += tstride) {
+      const int m0 = (t % p.m_blocks) * GBM, n0 = (t / p.m_blocks) * GBN;
       if (!mbar_wait(&acc_full[buf], aph, abort, &g_tc_err)) break;
       tc_fence_after();
       const int row = m0 + 32 * sp + lane;
@@ -232,8 +218,7 @@ __global__ void __launch_bounds__(GTHREADS, 1)
   }
 
   tc_fence_before();
-  __syncwarp();
-  cluster_sync_all();                            // the peer no longer writes into this CTA
+  __syncthreads();
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
@@ -605,36 +590,6 @@ static cudaError_t map_error(CUresult r) {
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-namespace {
-// Resident clusters of two GEMM CTAs on device `dev` (cached per kernel).
-int gemm_max_active_pairs(const void* kern, int dev) {
-  static std::mutex mu;
-  static std::map<std::pair<const void*, int>, int> cache;
-  std::lock_guard<std::mutex> lk(mu);
-  const auto key = std::make_pair(kern, dev);
-  auto it = cache.find(key);
-  if (it != cache.end()) return it->second;
-  cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(2);
-  cfg.blockDim = dim3(GTHREADS);
-  cfg.dynamicSmemBytes = GSMEM;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
-    cudaGetLastError();
-    n = 0;
-  }
-  cache[key] = n;
-  return n;
-}
-}  // namespace
-
 cudaError_t launch_tc_gemm(const void* a, const void* b, void* c, GemmShape sh, bool a_mn,
                            bool b_mn, bool c_f16, int num_sms, cudaStream_t stream) {
   CUtensorMap ta, tb;
@@ -647,12 +602,11 @@ cudaError_t launch_tc_gemm(const void* a, const void* b, void* c, GemmShape sh, 
     r = encode_tensor_map_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a, sh.M, sh.K,
                              static_cast<uint64_t>(sh.M) * 2, 64, GBK, CU_TENSOR_MAP_SWIZZLE_128B);
   if (r != CUDA_SUCCESS) return map_error(r);
-  // Bop is [K x N]; stored [N][K] (K-major) or [K][N] (MN-major). Each CTA of
-  // a pair loads half of the 256 B columns: one 128-row K-major box, or two of
-  // the four 64-column MN-major boxes.
+  // Bop is [K x N]; stored [N][K] (K-major: one 256-row box) or [K][N]
+  // (MN-major: four 64-column boxes).
   if (!b_mn)
     r = encode_tensor_map_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, b, sh.K, sh.N,
-                             static_cast<uint64_t>(sh.K) * 2, GBK, GBN / 2, CU_TENSOR_MAP_SWIZZLE_128B);
+                             static_cast<uint64_t>(sh.K) * 2, GBK, GBN, CU_TENSOR_MAP_SWIZZLE_128B);
   else
     r = encode_tensor_map_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, b, sh.N, sh.K,
                              static_cast<uint64_t>(sh.N) * 2, 64, GBK, CU_TENSOR_MAP_SWIZZLE_128B);
@@ -663,9 +617,9 @@ cudaError_t launch_tc_gemm(const void* a, const void* b, void* c, GemmShape sh, 
   p.M = sh.M;
   p.N = sh.N;
   p.K = sh.K;
-  p.m_pairs = (sh.M + 2 * GBM - 1) / (2 * GBM);
+  p.m_blocks = (sh.M + GBM - 1) / GBM;
   const int n_blocks = (sh.N + GBN - 1) / GBN;
-  p.pair_tiles = p.m_pairs * n_blocks;
+  p.tiles = p.m_blocks * n_blocks;
 
   cudaError_t e;
   const void* kern = nullptr;
@@ -679,27 +633,10 @@ cudaError_t launch_tc_gemm(const void* a, const void* b, void* c, GemmShape sh, 
 #undef KAIO_PICK_GEMM
   e = ensure_smem_limit(kern, static_cast<int>(GSMEM));
   if (e != cudaSuccess) return e;
-  // Persistent: as many CTA pairs as can be resident at once (pairs must sit
-  // in one GPC), capped by the number of tiles.
-  int dev = 0;
-  e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  const int slots = gemm_max_active_pairs(kern, dev);
-  const int pairs = std::max(1, std::min(p.pair_tiles, slots > 0 ? slots : num_sms / 2));
-  cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
-  cfg.blockDim = dim3(GTHREADS);
-  cfg.dynamicSmemBytes = GSMEM;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  // Persistent: one CTA per SM, capped by the number of tiles.
+  const int grid = std::max(1, std::min(p.tiles, num_sms));
   void* args[] = {&ta, &tb, &p};
-  e = cudaLaunchKernelExC(&cfg, kern, args);
+  e = cudaLaunchKernel(kern, dim3(static_cast<unsigned>(grid)), dim3(GTHREADS), args, GSMEM, stream);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

@@ -34,19 +34,8 @@ SHAPES = [
 ]
 
 
-@pytest.fixture(params=["auto", "mma", "streamk"])
-def decode_split(request, monkeypatch):
-    """Run a test under each decode kernel choice (the library reads
-    KAIO_DECODE_SPLIT on every call; both kernels must give the same result)."""
-    if request.param != "auto":
-        monkeypatch.setenv("KAIO_DECODE_SPLIT", request.param)
-    return request.param
-
-
 @pytest.mark.parametrize("m,n,k", SHAPES)
-def test_small_shapes(m, n, k, decode_split):
-    if m > 16 and decode_split != "auto":
-        pytest.skip("decode split choice applies to M <= 16")
+def test_small_shapes(m, n, k):
     check_full(qkv_inputs(m, n, k, seed=m * 7 + n + k), f"M={m} N={n} K={k}")
 
 
@@ -54,11 +43,11 @@ def test_config_m16_k256_n128_seed0():
     check_full(qkv_inputs(16, 128, 256, seed=0), "c1")
 
 
-def test_decode_m1_k4096_n4096_full(decode_split):
+def test_decode_m1_k4096_n4096_full():
     check_full(qkv_inputs(1, 4096, 4096, seed=0), "decode M=1")
 
 
-def test_batched_decode_m16_k8192_n8192_sampled_columns(decode_split):
+def test_batched_decode_m16_k8192_n8192_sampled_columns():
     inp = qkv_inputs(16, 8192, 8192, seed=0)
     got = run(inp)
     cols = np.sort(np.random.default_rng(0).choice(8192, 384, replace=False))
@@ -80,7 +69,7 @@ def test_prefill_4096_sampled_rows():
 
 
 @pytest.mark.parametrize("m", [4, 16, 96])
-def test_deterministic(m, decode_split):
+def test_deterministic(m):
     inp = qkv_inputs(m, 1032, 2048, seed=5)
     a = run(inp)
     b = run(inp)
@@ -89,7 +78,7 @@ def test_deterministic(m, decode_split):
 
 
 @pytest.mark.parametrize("m,n,k", [(5, 264, 256), (40, 136, 384)])
-def test_guard_bands_untouched(m, n, k, decode_split):
+def test_guard_bands_untouched(m, n, k):
     import torch
     inp = qkv_inputs(m, n, k, seed=3)
     ins = qkv_to_dev(inp)
@@ -176,7 +165,7 @@ def test_no_device_timeouts_reported():
 
 
 @pytest.mark.parametrize("m", [1, 16])
-def test_input_written_by_the_preceding_kernel(m, decode_split):
+def test_input_written_by_the_preceding_kernel(m):
     """A call must read x as left by the kernel just before it in the stream
     (the decode kernel may start early under programmatic dependent launch and
     must wait for its predecessor before reading): x is produced on the device
@@ -197,7 +186,7 @@ def test_input_written_by_the_preceding_kernel(m, decode_split):
         assert_qkv_close(to_host(o), r, f"preceding-kernel x {name}")
 
 
-def test_chained_calls_read_the_previous_calls_output(decode_split):
+def test_chained_calls_read_the_previous_calls_output():
     """Call 2 takes call 1's Q output as its x (K = N) with no host
     synchronisation between them: it must see all of call 1's output."""
     import torch

@@ -3,8 +3,9 @@
 It serves callers that cannot allocate device memory (engines and plugin hosts
 that own all device memory, fully reserved processes, latency-critical paths):
 its split-K scratch is a fixed array inside the library instead of a workspace
-the library allocates. Its results must match the regular entry point within
-the projection tolerance, on consecutive calls that share that array.
+the library would otherwise need. Its results must match both the regular entry
+point and the CPU oracle within the projection tolerance, element by element,
+on consecutive calls that share that array.
 
 This file is collected last so that a run stopping at the first failure has
 already run every other test; it also passes when run on its own.
@@ -36,7 +37,7 @@ def _close(got, ref):
 
 
 @pytest.mark.parametrize("m,n,k", [(16, 1032, 640), (1, 4096, 4096), (5, 264, 384)])
-def test_noalloc_matches_regular_entry_twice(m, n, k):
+def test_noalloc_matches_regular_entry_and_oracle_twice(m, n, k):
     import torch
     lib = kaio.lib()
     inp = qkv_inputs(m, n, k, seed=m + n + k)
@@ -44,13 +45,16 @@ def test_noalloc_matches_regular_entry_twice(m, n, k):
     ref_out = [torch.empty((m, n), dtype=torch.float16, device="cuda") for _ in range(3)]
     _call(lib.kaio_qkv_project_int4, ins, ref_out, m, n, k)
     torch.cuda.synchronize()
-    ref = [to_host(o) for o in ref_out]
+    regular = [to_host(o) for o in ref_out]
+    exact = oracle.qkv_project_int4_ref(*inp.__dict__.values())
     for _ in range(2):                       # two calls in a row share the scratch array
         out = [torch.full((m, n), float("nan"), dtype=torch.float16, device="cuda") for _ in range(3)]
         _call(lib.kaio_qkv_project_int4_noalloc, ins, out, m, n, k)
         torch.cuda.synchronize()
-        for o, r in zip(out, ref):
-            _close(to_host(o), r)
+        for o, r, e in zip(out, regular, exact):
+            got = to_host(o)
+            _close(got, r)                   # the regular entry point's result
+            _close(got, e)                   # the oracle's f64 result
 
 
 def test_noalloc_rejects_sizes_beyond_its_limits():
