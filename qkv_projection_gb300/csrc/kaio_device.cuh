@@ -391,6 +391,21 @@ __device__ __forceinline__ void dequant_natural(uint32_t word, uint32_t s2, uint
   out[3] = hmul2_rn(hsub2_rn(and_xor<kMixMask>(b32, kMixMagic), kMixMagic), s2);  // n6, n7
 }
 
+// K order inside a 16-byte chunk of staged f16 activations (8 K values) changed
+// from (0..7) to (0,4,1,5,2,6,3,7), the order in which PairedNibbles yields a
+// packed word's weights: a tensor-core operand pair and its activations must
+// agree on the K order, and a chunk's 16 bytes stay together under the 128-byte
+// swizzle, so the permutation is done in place wherever the chunk sits.
+__device__ __forceinline__ void permute_x_chunk(unsigned char* p) {
+  uint4 v = *reinterpret_cast<const uint4*>(p);
+  uint4 o;
+  o.x = __byte_perm(v.x, v.z, 0x5410);
+  o.y = __byte_perm(v.x, v.z, 0x7632);
+  o.z = __byte_perm(v.y, v.w, 0x5410);
+  o.w = __byte_perm(v.y, v.w, 0x7632);
+  *reinterpret_cast<uint4*>(p) = o;
+}
+
 // ---------------------------------------------------------------------------
 // INT8 -> f16, exact (every int8 value is an f16 integer).
 //

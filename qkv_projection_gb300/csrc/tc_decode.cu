@@ -84,19 +84,6 @@ struct DecTcParams {
   int sbox;      // scale rows per TMA box
 };
 
-// K order inside every 16-byte chunk of a staged x box is changed from
-// (0..7) to (0,4,1,5,2,6,3,7): the dequantised weights come out of the mask
-// trick as nibble pairs (j, j+4), and A and B must agree on the K order.
-__device__ __forceinline__ void permute_x_chunk(unsigned char* p) {
-  uint4 v = *reinterpret_cast<const uint4*>(p);
-  uint4 o;
-  o.x = __byte_perm(v.x, v.z, 0x5410);
-  o.y = __byte_perm(v.x, v.z, 0x7632);
-  o.z = __byte_perm(v.y, v.w, 0x5410);
-  o.w = __byte_perm(v.y, v.w, 0x7632);
-  *reinterpret_cast<uint4*>(p) = o;
-}
-
 template <int kBits>
 __global__ void __launch_bounds__(DTHREADS, 1)
     tc_decode_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW0,

@@ -411,16 +411,13 @@ __global__ void __launch_bounds__(PTHREADS, 1)
         }
         (void)ss;
         for (int hh = 0; hh < 2; ++hh) {
-          if (!mbar_wait(&a_empty[a], aph ^ 1, abort, &g_tc_err)) { ok = false; break; }
-          // A stage 1 is free once the MMAs of the previous k-step's second
-          // half have completed, i.e. every MMA reading that k-step's x tile:
-          // one warp releases its shared-memory stage on the MMA's behalf.
-          if (hh == 1 && rel_st >= 0 && warp == 1 + PMMA_WARPS && lane == 0) mbar_arrive(&empty[rel_st]);
-          tc_fence_after();
+          // Convert this warp's 16 K of the half into registers first: only the
+          // stores need the A stage, so the conversion overlaps the MMAs still
+          // reading it. Column q*16 + hf*8 + c of the A stage holds K pair c of
+          // this warp's 16 K of projection q.
+          uint32_t v[3][8];
 #pragma unroll
           for (int q = 0; q < 3; ++q) {
-            // column q*16 + hf*8 + c of the A stage holds K pair c of this warp's 16 K
-            uint32_t v[8];
             if constexpr (kBits == 4) {
               const int r0 = hh * 4 + hf * 2;
               const uint32_t w0 = sw[q * (PW_BYTES / 4) + r0 * PBN + nl];
@@ -430,17 +427,25 @@ __global__ void __launch_bounds__(PTHREADS, 1)
               dequant_natural(w1, s2[q], v1);
 #pragma unroll
               for (int c = 0; c < 4; ++c) {
-                v[c] = v0[c];
-                v[4 + c] = v1[c];
+                v[q][c] = v0[c];
+                v[q][4 + c] = v1[c];
               }
             } else {
               const int r0 = hh * 8 + hf * 4;
 #pragma unroll
               for (int j = 0; j < 4; ++j)
-                int8x4_to_half2x2(sw[q * (PW_BYTES / 4) + (r0 + j) * PBN + nl], v[2 * j], v[2 * j + 1]);
+                int8x4_to_half2x2(sw[q * (PW_BYTES / 4) + (r0 + j) * PBN + nl], v[q][2 * j], v[q][2 * j + 1]);
             }
-            tmem_st8(tmem + lane_base + PA_COL0 + a * PA_STAGE_COLS + q * 16 + hf * 8, v);
           }
+          if (!mbar_wait(&a_empty[a], aph ^ 1, abort, &g_tc_err)) { ok = false; break; }
+          // A stage 1 is free once the MMAs of the previous k-step's second
+          // half have completed, i.e. every MMA reading that k-step's x tile:
+          // one warp releases its shared-memory stage on the MMA's behalf.
+          if (hh == 1 && rel_st >= 0 && warp == 1 + PMMA_WARPS && lane == 0) mbar_arrive(&empty[rel_st]);
+          tc_fence_after();
+#pragma unroll
+          for (int q = 0; q < 3; ++q)
+            tmem_st8(tmem + lane_base + PA_COL0 + a * PA_STAGE_COLS + q * 16 + hf * 8, v[q]);
           tmem_st_wait();
           tc_fence_before();
           __syncwarp();
