@@ -254,8 +254,8 @@ int kaio_dequantize_per_group(int q_dtype, int dtype, int32_t outer, int32_t axi
  * A test entry for bit-exact comparison of the dequant stage.
  *
  *   w  u32 [K/8, N],  s  f16 [K/128, N],  out  f16 [K, N]
- *   variant 0: the K-row-order routine of the tensor-core kernel
- *   variant 1: the paired-nibble routine of the decode kernel
+ *   variant 0: the K-row-order routine of the tile kernel (M >= 17)
+ *   variant 1: the paired-nibble routine of the decode kernel (M <= 16)
  * Errors: as kaio_qkv_project_int4 for K and N; variant not 0 or 1.
  */
 int kaio_dequant_int4_debug(const uint32_t* w, const void* s, void* out, uint32_t K, uint32_t N,
