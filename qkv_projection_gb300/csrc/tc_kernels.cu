@@ -45,61 +45,78 @@ __device__ unsigned g_tc_err = 0;
 namespace {
 
 // ============================================================== dense GEMM
-constexpr int GBM = 128, GBN = 256, GBK = 64, GSTAGES = 4;
+// A CTA pair computes a 256 x 256 tile of C with one tcgen05.mma of M = 256
+// per 16 K (cta_group::2): CTA rank r loads A rows m0 + 128r .. +127 and B
+// columns n0 + 128r .. +127 into its own shared memory and holds C rows
+// m0 + 128r .. +127 (all 256 columns) in its tensor memory. B is read once per
+// pair, and each SM's shared memory holds half of the B tile.
+constexpr int GBM = 128;                       // rows of A (and of C) per CTA
+constexpr int GBN = 256;                       // columns of C per pair tile
+constexpr int GBK = 64, GSTAGES = 6;
 constexpr int GA_BYTES = GBM * GBK * 2;        // 16 KB
-constexpr int GB_BYTES = GBN * GBK * 2;        // 32 KB
+constexpr int GB_BYTES = (GBN / 2) * GBK * 2;  // 16 KB: this CTA's half of B
 constexpr int GSTAGE_BYTES = GA_BYTES + GB_BYTES;
-constexpr int GTHREADS = 192;                  // w0 TMA, w1 MMA, w2..5 epilogue
+constexpr int GTHREADS = 192;                  // w0 TMA, w1 MMA (rank 0) + TMEM, w2..5 epilogue
 constexpr uint32_t GTMEM_COLS = 512;           // 2 x 256 f32 accumulators
 constexpr size_t GSMEM = static_cast<size_t>(GSTAGES) * GSTAGE_BYTES + 1024;
 
 struct GemmParams {
   void* c;              // f32 or f16 [M, N]
   int M, N, K;
-  int m_blocks, tiles;  // 128-row blocks; (128-row, 256-column) tiles
+  int m_pairs, tiles;   // 256-row blocks; (256-row, 256-column) pair tiles
 };
 
 // C16: the epilogue rounds the f32 accumulators to f16 (round-to-nearest-even)
 // and stores f16, fusing the cast the page's backward applies afterwards.
 //
-// Persistent: CTA c takes tiles c, c + grid, ...; tiles are numbered down the
-// rows first, so the CTAs running at one time share few B tiles, which L2 serves.
+// Barriers: both CTAs' stage bytes are counted on rank 0's full[st] (rank 0's
+// producer expects them all; the pair form of the TMA load lets rank 1's
+// copies complete there); rank 0's MMA thread releases stage st in both CTAs and hands each CTA its accumulator with
+// commits to each CTA's own barriers; both CTAs' epilogue warps arrive on rank
+// 0's acc_empty. Persistent: pair p takes tiles p, p + pairs, ...; tiles are
+// numbered down the rows first, so the pairs running at one time share B tiles
+// through L2.
 template <bool A_MN, bool B_MN, bool C16>
 __global__ void __launch_bounds__(GTHREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const GemmParams p) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = align_smem_1024(smem_raw);
-  __shared__ __align__(8) uint64_t full[GSTAGES], empty[GSTAGES], acc_full[2], acc_empty[2],
-      mma_done;
+  __shared__ __align__(8) uint64_t full[GSTAGES], empty[GSTAGES], acc_full[2], acc_empty[2], mma_done;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rank = static_cast<int>(cluster_ctarank());
   if (threadIdx.x == 0) {
     for (int s = 0; s < GSTAGES; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);                   // the MMA thread's commit
+      mbar_init(&full[s], 1);                  // rank 0's: its producer's expect_tx for both CTAs' bytes
+      mbar_init(&empty[s], 1);                 // rank 0's MMA commit
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&acc_full[b], 1);
-      mbar_init(&acc_empty[b], 4);
+      mbar_init(&acc_full[b], 1);              // rank 0's MMA commit
+      mbar_init(&acc_empty[b], 8);             // rank 0's: 4 epilogue warps of each CTA
     }
     mbar_init(&mma_done, 1);
     abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(&tmem_base_sh, GTMEM_COLS);
-    tmem_relinquish();
+    tmem_alloc_pair(&tmem_base_sh, GTMEM_COLS);
+    tmem_relinquish_pair();
   }
   tc_fence_before();
-  __syncthreads();
+  __syncwarp();
+  cluster_sync_all();                          // both CTAs' barriers exist before any remote use
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
   const int nk = (p.K + GBK - 1) / GBK;
   volatile int* abort = &abort_flag;
-  const int tstride = static_cast<int>(gridDim.x);
+  const int pair = static_cast<int>(blockIdx.x) >> 1;
+  const int pstride = static_cast<int>(gridDim.x) >> 1;
+  // rank 0's copy of a barrier of this CTA, and the peer's copy
+  auto at_rank0 = [&](uint64_t* bar) { return dsmem_map(smem_u32(bar), 0); };
+  auto at_peer = [&](uint64_t* bar) { return dsmem_map(smem_u32(bar), static_cast<uint32_t>(rank ^ 1)); };
 
   if (warp == 0) {
     if (lane == 0) {
@@ -107,49 +124,57 @@ __global__ void __launch_bounds__(GTHREADS, 1)
       tma_prefetch_desc(&tmB);
       int st = 0;
       uint32_t ph = 0;
-      uint32_t fills[GSTAGES] = {0, 0, 0, 0};
-      for (int t = static_cast<int>(blockIdx.x); t < p.tiles; t += tstride) {
-        const int m0 = (t % p.m_blocks) * GBM, n0 = (t / p.m_blocks) * GBN;
+      uint32_t fills[GSTAGES] = {};
+      for (int t = pair; t < p.tiles; t += pstride) {
+        const int m0 = (t % p.m_pairs) * (2 * GBM) + rank * GBM;
+        const int n0 = (t / p.m_pairs) * GBN + rank * (GBN / 2);
         for (int kb = 0; kb < nk; ++kb) {
-          if (!mbar_wait(&empty[st], ph ^ 1, abort, &g_tc_err)) goto producer_done;
+          if (!mbar_wait_cluster(&empty[st], ph ^ 1, abort, &g_tc_err)) goto producer_done;
           ++fills[st];
           unsigned char* sa = smem + st * GSTAGE_BYTES;
           unsigned char* sb = sa + GA_BYTES;
-          mbar_arrive_expect_tx(&full[st], GSTAGE_BYTES);
+          // Only rank 0's producer arrives (expecting both CTAs' bytes); rank
+          // 1's copies count their bytes on rank 0's barrier directly. A
+          // thread's arrive on another CTA's barrier stalls it for about as long
+          // as a k-step takes, so no thread makes one per k-step.
+          const uint32_t fb = at_rank0(&full[st]);
+          if (rank == 0) mbar_arrive_expect_tx(&full[st], 2 * GSTAGE_BYTES);
           if (!A_MN) {
-            tma_load_2d(sa, &tmA, &full[st], kb * GBK, m0);
+            tma_load_2d_pair(sa, &tmA, fb, kb * GBK, m0);
           } else {
-            tma_load_2d(sa, &tmA, &full[st], m0, kb * GBK);
-            tma_load_2d(sa + 8192, &tmA, &full[st], m0 + 64, kb * GBK);
+            tma_load_2d_pair(sa, &tmA, fb, m0, kb * GBK);
+            tma_load_2d_pair(sa + 8192, &tmA, fb, m0 + 64, kb * GBK);
           }
           if (!B_MN) {
-            tma_load_2d(sb, &tmB, &full[st], kb * GBK, n0);
+            tma_load_2d_pair(sb, &tmB, fb, kb * GBK, n0);
           } else {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) tma_load_2d(sb + q * 8192, &tmB, &full[st], n0 + 64 * q, kb * GBK);
+            tma_load_2d_pair(sb, &tmB, fb, n0, kb * GBK);
+            tma_load_2d_pair(sb + 8192, &tmB, fb, n0 + 64, kb * GBK);
           }
           if (++st == GSTAGES) { st = 0; ph ^= 1; }
         }
       }
     producer_done:
-      // No copy may still be landing in shared memory when the CTA exits.
+      // No copy may still be landing in this CTA's shared memory when it
+      // exits: every fill is consumed by an MMA (which waited for its bytes)
+      // before its release reaches this CTA's stage.
       for (int s2 = 0; s2 < GSTAGES; ++s2)
-        if (fills[s2]) mbar_wait_drain(&full[s2], (fills[s2] - 1) & 1, &g_tc_err);
+        if (fills[s2]) mbar_wait_cluster_drain(&empty[s2], (fills[s2] - 1) & 1, &g_tc_err);
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_f16_f32(GBM, GBN, A_MN, B_MN);
+    if (rank == 0 && lane == 0) {
+      constexpr uint32_t idesc = idesc_f16_f32(2 * GBM, GBN, A_MN, B_MN);
       int st = 0;
       uint32_t ph = 0;
       int buf = 0;
       uint32_t aph = 0;
-      for (int t = static_cast<int>(blockIdx.x); t < p.tiles; t += tstride) {
-        if (!mbar_wait(&acc_empty[buf], aph ^ 1, abort, &g_tc_err)) break;
+      for (int t = pair; t < p.tiles; t += pstride) {
+        if (!mbar_wait_cluster(&acc_empty[buf], aph ^ 1, abort, &g_tc_err)) break;
         tc_fence_after();
         const uint32_t d = tmem + buf * GBN;
         bool ok = true;
         for (int kb = 0; kb < nk; ++kb) {
-          if (!mbar_wait(&full[st], ph, abort, &g_tc_err)) { ok = false; break; }
+          if (!mbar_wait_cluster(&full[st], ph, abort, &g_tc_err)) { ok = false; break; }
           tc_fence_after();
           const uint32_t sa = smem_u32(smem + st * GSTAGE_BYTES);
           const uint32_t sb = sa + GA_BYTES;
@@ -159,27 +184,30 @@ __global__ void __launch_bounds__(GTHREADS, 1)
                                      : sdesc_sw128(sa + kk * 32, 16, 1024);
             const uint64_t bd = B_MN ? sdesc_sw128(sb + kk * 2048, 8192, 1024)
                                      : sdesc_sw128(sb + kk * 32, 16, 1024);
-            umma_ss(d, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+            umma_ss_pair(d, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
           }
-          umma_commit(&empty[st]);
+          umma_commit_pair(smem_u32(&empty[st]));
+          umma_commit_pair(at_peer(&empty[st]));
           if (++st == GSTAGES) { st = 0; ph ^= 1; }
         }
         if (!ok) break;
-        umma_commit(&acc_full[buf]);
+        umma_commit_pair(smem_u32(&acc_full[buf]));
+        umma_commit_pair(at_peer(&acc_full[buf]));
         if (++buf == 2) { buf = 0; aph ^= 1; }
       }
-      // Every MMA issued has completed before TMEM is released.
-      umma_commit(&mma_done);
-      mbar_wait_drain(&mma_done, 0, &g_tc_err);
+      // Every MMA issued (and with it every commit to either CTA) has
+      // completed before TMEM is released.
+      umma_commit_pair(smem_u32(&mma_done));
+      mbar_wait_cluster_drain(&mma_done, 0, &g_tc_err);
     }
   } else {
-    // Epilogue: warp w drains TMEM lanes 32*(w%4) .. +31 (rows of the tile).
+    // Epilogue: warp w drains TMEM lanes 32*(w%4) .. +31 (rows of this CTA's half).
     const int sp = warp & 3;
     int buf = 0;
     uint32_t aph = 0;
-    for (int t = static_cast<int>(blockIdx.x); t < p.tiles; t += tstride) {
-      const int m0 = (t % p.m_blocks) * GBM, n0 = (t / p.m_blocks) * GBN;
-      if (!mbar_wait(&acc_full[buf], aph, abort, &g_tc_err)) break;
+    for (int t = pair; t < p.tiles; t += pstride) {
+      const int m0 = (t % p.m_pairs) * (2 * GBM) + rank * GBM, n0 = (t / p.m_pairs) * GBN;
+      if (!mbar_wait_cluster(&acc_full[buf], aph, abort, &g_tc_err)) break;
       tc_fence_after();
       const int row = m0 + 32 * sp + lane;
 #pragma unroll 1
@@ -212,17 +240,18 @@ __global__ void __launch_bounds__(GTHREADS, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&acc_empty[buf]);
+      if (lane == 0) mbar_arrive_cluster(at_rank0(&acc_empty[buf]));
       if (++buf == 2) { buf = 0; aph ^= 1; }
     }
   }
 
   tc_fence_before();
-  __syncthreads();
+  __syncwarp();
+  cluster_sync_all();                          // no remote arrive or commit targets an exited CTA
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem, GTMEM_COLS);
+    tmem_dealloc_pair(tmem, GTMEM_COLS);
   }
 }
 
@@ -595,6 +624,36 @@ static cudaError_t map_error(CUresult r) {
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+namespace {
+// Resident clusters of two GEMM CTAs on device `dev` (cached per kernel).
+int gemm_max_active_pairs(const void* kern, int dev) {
+  static std::mutex mu;
+  static std::map<std::pair<const void*, int>, int> cache;
+  std::lock_guard<std::mutex> lk(mu);
+  const auto key = std::make_pair(kern, dev);
+  auto it = cache.find(key);
+  if (it != cache.end()) return it->second;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(2);
+  cfg.blockDim = dim3(GTHREADS);
+  cfg.dynamicSmemBytes = GSMEM;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    n = 0;
+  }
+  cache[key] = n;
+  return n;
+}
+}  // namespace
+
 cudaError_t launch_tc_gemm(const void* a, const void* b, void* c, GemmShape sh, bool a_mn,
                            bool b_mn, bool c_f16, int num_sms, cudaStream_t stream) {
   CUtensorMap ta, tb;
@@ -607,11 +666,12 @@ cudaError_t launch_tc_gemm(const void* a, const void* b, void* c, GemmShape sh, 
     r = encode_tensor_map_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a, sh.M, sh.K,
                              static_cast<uint64_t>(sh.M) * 2, 64, GBK, CU_TENSOR_MAP_SWIZZLE_128B);
   if (r != CUDA_SUCCESS) return map_error(r);
-  // Bop is [K x N]; stored [N][K] (K-major: one 256-row box) or [K][N]
-  // (MN-major: four 64-column boxes).
+  // Bop is [K x N]; stored [N][K] (K-major) or [K][N] (MN-major). Each CTA of
+  // a pair loads its 128 columns: one 128-row K-major box, or two 64-column
+  // MN-major boxes.
   if (!b_mn)
     r = encode_tensor_map_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, b, sh.K, sh.N,
-                             static_cast<uint64_t>(sh.K) * 2, GBK, GBN, CU_TENSOR_MAP_SWIZZLE_128B);
+                             static_cast<uint64_t>(sh.K) * 2, GBK, GBN / 2, CU_TENSOR_MAP_SWIZZLE_128B);
   else
     r = encode_tensor_map_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, b, sh.N, sh.K,
                              static_cast<uint64_t>(sh.N) * 2, 64, GBK, CU_TENSOR_MAP_SWIZZLE_128B);
@@ -622,9 +682,9 @@ cudaError_t launch_tc_gemm(const void* a, const void* b, void* c, GemmShape sh, 
   p.M = sh.M;
   p.N = sh.N;
   p.K = sh.K;
-  p.m_blocks = (sh.M + GBM - 1) / GBM;
+  p.m_pairs = (sh.M + 2 * GBM - 1) / (2 * GBM);
   const int n_blocks = (sh.N + GBN - 1) / GBN;
-  p.tiles = p.m_blocks * n_blocks;
+  p.tiles = p.m_pairs * n_blocks;
 
   cudaError_t e;
   const void* kern = nullptr;
@@ -638,10 +698,27 @@ cudaError_t launch_tc_gemm(const void* a, const void* b, void* c, GemmShape sh, 
 #undef KAIO_PICK_GEMM
   e = ensure_smem_limit(kern, static_cast<int>(GSMEM));
   if (e != cudaSuccess) return e;
-  // Persistent: one CTA per SM, capped by the number of tiles.
-  const int grid = std::max(1, std::min(p.tiles, num_sms));
+  // Persistent: as many CTA pairs as can be resident at once (a pair sits in
+  // one GPC), capped by the number of tiles.
+  int dev = 0;
+  e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const int slots = gemm_max_active_pairs(kern, dev);
+  const int pairs = std::max(1, std::min(p.tiles, slots > 0 ? slots : num_sms / 2));
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
+  cfg.blockDim = dim3(GTHREADS);
+  cfg.dynamicSmemBytes = GSMEM;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   void* args[] = {&ta, &tb, &p};
-  e = cudaLaunchKernel(kern, dim3(static_cast<unsigned>(grid)), dim3(GTHREADS), args, GSMEM, stream);
+  e = cudaLaunchKernelExC(&cfg, kern, args);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
