@@ -56,7 +56,8 @@ constexpr int GBK = 64, GSTAGES = 6;
 constexpr int GA_BYTES = GBM * GBK * 2;        // 16 KB
 constexpr int GB_BYTES = (GBN / 2) * GBK * 2;  // 16 KB: this CTA's half of B
 constexpr int GSTAGE_BYTES = GA_BYTES + GB_BYTES;
-constexpr int GTHREADS = 192;                  // w0 TMA, w1 MMA (rank 0) + TMEM, w2..5 epilogue
+constexpr int GTHREADS = 224;                  // w0, w6 TMA; w1 MMA (rank 0) + TMEM; w2..5 epilogue
+static_assert(GSTAGES % 2 == 0, "the two producers own alternate stages");
 constexpr uint32_t GTMEM_COLS = 512;           // 2 x 256 f32 accumulators
 constexpr size_t GSMEM = static_cast<size_t>(GSTAGES) * GSTAGE_BYTES + 1024;
 
@@ -118,8 +119,12 @@ __global__ void __launch_bounds__(GTHREADS, 1)
   auto at_rank0 = [&](uint64_t* bar) { return dsmem_map(smem_u32(bar), 0); };
   auto at_peer = [&](uint64_t* bar) { return dsmem_map(smem_u32(bar), static_cast<uint32_t>(rank ^ 1)); };
 
-  if (warp == 0) {
+  if (warp == 0 || warp == 6) {
+    // Two producer threads, one per warp, take alternate k-steps (and so
+    // alternate stages): a thread spends several hundred cycles per stage on
+    // its barrier operations and copies, and two of them keep the ring full.
     if (lane == 0) {
+      const int pid = warp == 0 ? 0 : 1;
       tma_prefetch_desc(&tmA);
       tma_prefetch_desc(&tmB);
       int st = 0;
@@ -129,6 +134,10 @@ __global__ void __launch_bounds__(GTHREADS, 1)
         const int m0 = (t % p.m_pairs) * (2 * GBM) + rank * GBM;
         const int n0 = (t / p.m_pairs) * GBN + rank * (GBN / 2);
         for (int kb = 0; kb < nk; ++kb) {
+          if ((st & 1) != pid) {                 // the other producer's stage
+            if (++st == GSTAGES) { st = 0; ph ^= 1; }
+            continue;
+          }
           if (!mbar_wait_cluster(&empty[st], ph ^ 1, abort, &g_tc_err)) goto producer_done;
           ++fills[st];
           unsigned char* sa = smem + st * GSTAGE_BYTES;
@@ -200,7 +209,7 @@ __global__ void __launch_bounds__(GTHREADS, 1)
       umma_commit_pair(smem_u32(&mma_done));
       mbar_wait_cluster_drain(&mma_done, 0, &g_tc_err);
     }
-  } else {
+  } else if (warp <= 5) {
     // Epilogue: warp w drains TMEM lanes 32*(w%4) .. +31 (rows of this CTA's half).
     const int sp = warp & 3;
     int buf = 0;
