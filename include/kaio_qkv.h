@@ -118,6 +118,27 @@ int kaio_qkv_project_int4_noalloc(const void* x, const uint32_t* wq, const uint3
                                   uint32_t N, uint32_t K, kaio_stream_t stream);
 
 /*
+ * Test entry for the bounded waits of the decode kernel (the failure detection
+ * of "baracuda-kernels -- src/quantize/dequantize_per_group_backward.rs",
+ * run -> map_status: a failure surfaces as a status, never as a hang).
+ *
+ * Runs the kernel kaio_qkv_project_int4 runs for M <= 16, with every wait of
+ * its pipeline limited to wait_limit_ns instead of 2 s. With a limit shorter
+ * than the pipeline's hand-offs (0 makes the first wait that finds its phase
+ * incomplete give up), the kernel records a timeout in the device error word,
+ * lets the copies and MMAs already in flight finish, frees its tensor memory
+ * and returns; the outputs are then undefined. The next kaio_device_status()
+ * reports KAIO_ERR_DEVICE_TIMEOUT and clears the word; the context stays
+ * usable. Arguments and errors as kaio_qkv_project_int4, with 1 <= M <= 16,
+ * K and N positive.
+ */
+int kaio_debug_decode_wait_limit(const void* x, const uint32_t* wq, const uint32_t* wk,
+                                 const uint32_t* wv, const void* sq, const void* sk,
+                                 const void* sv, void* q, void* k, void* v, uint32_t M,
+                                 uint32_t N, uint32_t K, uint64_t wait_limit_ns,
+                                 kaio_stream_t stream);
+
+/*
  * W8A16 fused tri-output QKV projection, the INT8 sibling of
  * kaio_qkv_project_int4. ("kaio-candle -- src/qkv_project_int4.rs", module
  * doc: the INT4 op follows the INT8 op's direct-call pattern but takes seven

@@ -236,6 +236,45 @@ int kaio_qkv_project_int4(const void* x, const uint32_t* wq, const uint32_t* wk,
   return KAIO_OK;
 }
 
+int kaio_debug_decode_wait_limit(const void* x, const uint32_t* wq, const uint32_t* wk, const uint32_t* wv,
+                                 const void* sq, const void* sk, const void* sv, void* q, void* k, void* v,
+                                 uint32_t M, uint32_t N, uint32_t K, uint64_t wait_limit_ns,
+                                 kaio_stream_t stream_) {
+  g_last_error.clear();
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  const size_t m = M, n = N, kk = K;
+  const Span in[7] = {{"x", x, m * kk * 2},          {"w_q_packed", wq, kk / 8 * n * 4},
+                      {"w_k_packed", wk, kk / 8 * n * 4}, {"w_v_packed", wv, kk / 8 * n * 4},
+                      {"scales_q", sq, kk / 128 * n * 2}, {"scales_k", sk, kk / 128 * n * 2},
+                      {"scales_v", sv, kk / 128 * n * 2}};
+  const Span out[3] = {{"q", q, m * n * 2}, {"k", k, m * n * 2}, {"v", v, m * n * 2}};
+  KAIO_TRY(check_not_null(in, 7));
+  KAIO_TRY(check_not_null(out, 3));
+  if (M == 0 || M > 16)
+    return fail(KAIO_ERR_INVALID_VALUE, "M (%u) must be 1..16: this entry runs the decode kernel", M);
+  if (K == 0 || K % 128 != 0)
+    return fail(KAIO_ERR_INVALID_VALUE, "K (%u) must be a positive multiple of group_size (128)", K);
+  if (N == 0 || N % 8 != 0)
+    return fail(KAIO_ERR_INVALID_VALUE, "N (%u) must be a positive multiple of 8", N);
+  bool run;
+  int dev;
+  DeviceInfo info;
+  KAIO_TRY(check_projection(in, 7, out, static_cast<uint64_t>(K) / 8 * N, M, N, K, stream, &run, &dev, &info));
+  if (!run) return KAIO_OK;
+  const kaio::TcDecodePlan tp = kaio::plan_tc_decode(static_cast<int>(M), static_cast<int>(N),
+                                                     static_cast<int>(K), dev);
+  if (!tp.ok) return fail(KAIO_ERR_CUDA, "no resident launch shape for the decode kernel");
+  const uint32_t* w3[3] = {wq, wk, wv};
+  const __half* s3[3] = {static_cast<const __half*>(sq), static_cast<const __half*>(sk),
+                         static_cast<const __half*>(sv)};
+  __half* o3[3] = {static_cast<__half*>(q), static_cast<__half*>(k), static_cast<__half*>(v)};
+  const cudaError_t e = kaio::launch_tc_decode_wait_limit(static_cast<const __half*>(x), w3, s3, o3,
+                                                          static_cast<int>(M), static_cast<int>(N),
+                                                          static_cast<int>(K), tp, wait_limit_ns, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "tcgen05 decode kernel launch");
+  return KAIO_OK;
+}
+
 int kaio_qkv_project_int8(const void* x, const uint32_t* wq, const uint32_t* wk, const uint32_t* wv,
                           float scale_q, float scale_k, float scale_v, void* q, void* k, void* v,
                           uint32_t M, uint32_t N, uint32_t K, kaio_stream_t stream_) {

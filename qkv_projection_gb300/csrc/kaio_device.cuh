@@ -120,6 +120,25 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
+// mbar_wait with a per-launch limit. At the normal limit (kWaitLimitNs) it is
+// mbar_wait. A shorter limit (a test of the timeout path) polls without
+// blocking, so that the limit, not the phase's completion, ends an unfinished
+// wait: the first poll that finds the phase incomplete after `limit_ns` gives up.
+__device__ __forceinline__ bool mbar_wait_lim(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                              unsigned* err, uint64_t limit_ns) {
+  if (limit_ns >= kWaitLimitNs) return mbar_wait(bar, parity, abort, err);
+  const uint64_t t0 = globaltimer();
+  for (;;) {
+    if (mbar_test_wait(bar, parity)) return true;
+    if (*abort) return false;
+    if (globaltimer() - t0 >= limit_ns) {
+      *abort = 1;
+      atomicOr(err, kDevErrTimeout);
+      return false;
+    }
+  }
+}
+
 // Wind-down wait: like mbar_wait but ignores the abort flag (used to let
 // copies or MMAs already in flight finish before the CTA frees its resources).
 __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, unsigned* err) {

@@ -62,6 +62,11 @@ TcDecodePlan plan_tc_decode(int M, int N, int K, int dev);
 cudaError_t launch_tc_decode(const __half* x, const uint32_t* const w[3], const __half* const s[3],
                              __half* const out[3], int M, int N, int K, const TcDecodePlan& pl,
                              cudaStream_t stream);
+// The INT4 decode kernel with every pipeline wait limited to wait_ns (a test
+// of the bounded-wait timeout path; the regular launch uses 2 s).
+cudaError_t launch_tc_decode_wait_limit(const __half* x, const uint32_t* const w[3], const __half* const s[3],
+                                        __half* const out[3], int M, int N, int K, const TcDecodePlan& pl,
+                                        unsigned long long wait_ns, cudaStream_t stream);
 // The same kernel for INT8 weights u32[K/4, N] (byte i = K-row 4r+i) with
 // one f32 scale per projection.
 TcDecodePlan plan_tc_decode_int8(int M, int N, int K, int dev);

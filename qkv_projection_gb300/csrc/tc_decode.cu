@@ -82,6 +82,7 @@ struct DecTcParams {
   int nst;       // ring stages (DGPS K groups each)
   int s_off;     // byte offset of the scale rows (after the ring)
   int sbox;      // scale rows per TMA box
+  unsigned long long wait_ns;   // limit of every pipeline wait (kWaitLimitNs; shorter in a test)
 };
 
 template <int kBits>
@@ -199,10 +200,10 @@ __global__ void __launch_bounds__(DTHREADS, 1)
     // and four 2 KB x boxes; the scale rows of the whole K range (issued above
     // with the first two stages).
     if (lane == 0) {
-      bool ok = pi >= nstg || pi >= p.nst || mbar_wait(&full[0], 0, abort, &g_td_err);
+      bool ok = pi >= nstg || pi >= p.nst || mbar_wait_lim(&full[0], 0, abort, &g_td_err, p.wait_ns);
       while (ok && pi < nstg && pi < p.nst) issue_stage();   // the rest of the first ring
       while (ok && pi < nstg) {
-        if (!mbar_wait(&empty[pst], pph ^ 1, abort, &g_td_err)) break;
+        if (!mbar_wait_lim(&empty[pst], pph ^ 1, abort, &g_td_err, p.wait_ns)) break;
         issue_stage();
       }
       for (int s2 = 0; s2 < p.nst; ++s2)
@@ -230,7 +231,7 @@ __global__ void __launch_bounds__(DTHREADS, 1)
       const uint32_t blo = static_cast<uint32_t>(bd0), bhi = static_cast<uint32_t>(bd0 >> 32);
       const int ngs = min(DGPS, nsg - i * DGPS);
       for (int j = 0; j < ngs; ++j) {              // K groups of this stage
-        if (!mbar_wait(&a_full[a], aph, abort, &g_td_err)) { ok = false; break; }
+        if (!mbar_wait_lim(&a_full[a], aph, abort, &g_td_err, p.wait_ns)) { ok = false; break; }
         if (lane == 0) {
           tc_fence_after();
           const uint32_t acc0 = (i | j) != 0 ? 1u : 0u;
@@ -274,7 +275,7 @@ __global__ void __launch_bounds__(DTHREADS, 1)
     const unsigned char* scale_base = smem + p.s_off + nl * 2;
     int st = 0;
     uint32_t aph = 0, ph = 0;
-    bool ok = nsb == 0 || mbar_wait(&sbar0, 0, abort, &g_td_err);
+    bool ok = nsb == 0 || mbar_wait_lim(&sbar0, 0, abort, &g_td_err, p.wait_ns);
     bool have_scales = nsb <= 1;                 // rows of the later scale boxes have landed
     // x chunks this thread permutes in its groups: the two 64-K boxes 2js and
     // 2js+1 of a group hold 2 x 16 rows x 8 chunks = 256 chunks, two per
@@ -286,7 +287,7 @@ __global__ void __launch_bounds__(DTHREADS, 1)
     for (int i = 0; i < nstg && ok; ++i) {
       const int ngs = min(DGPS, nsg - i * DGPS);
       if (js < ngs) {
-        if (!mbar_wait(&full[st], ph, abort, &g_td_err)) { ok = false; break; }
+        if (!mbar_wait_lim(&full[st], ph, abort, &g_td_err, p.wait_ns)) { ok = false; break; }
         if (kBits == 4 && pm < p.M) {
           permute_x_chunk(smem + st * DSTAGE_BYTES + poff);
           permute_x_chunk(smem + st * DSTAGE_BYTES + poff + DXBOX);
@@ -296,7 +297,7 @@ __global__ void __launch_bounds__(DTHREADS, 1)
           // Thread = column nl: its 32 packed rows of the group per projection,
           // converted exactly to f16 K pairs. Column c of projection q's 64 holds
           // K pair c (K-rows 2c, 2c+1: byte pair c % 2 of packed row c / 2).
-          if (!mbar_wait(&a_empty[js], aph ^ 1, abort, &g_td_err)) { ok = false; break; }
+          if (!mbar_wait_lim(&a_empty[js], aph ^ 1, abort, &g_td_err, p.wait_ns)) { ok = false; break; }
           tc_fence_after();
           const uint32_t* sw = reinterpret_cast<const uint32_t*>(smem + st * DSTAGE_BYTES + DX_STAGE) +
                                js * F::kRows * DN + nl;
@@ -322,7 +323,7 @@ __global__ void __launch_bounds__(DTHREADS, 1)
         }
         const int gl = i * DGPS + js;             // group index inside the CTA's range
         if (!have_scales && gl >= p.sbox) {
-          if (!mbar_wait(&sbar, 0, abort, &g_td_err)) { ok = false; break; }
+          if (!mbar_wait_lim(&sbar, 0, abort, &g_td_err, p.wait_ns)) { ok = false; break; }
           have_scales = true;
         }
         // scale rows of group gl: box gl/8 (boxes hold up to 8 rows), row gl%8
@@ -339,7 +340,7 @@ __global__ void __launch_bounds__(DTHREADS, 1)
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[st]);   // this set's words of the stage are in registers
-        if (!mbar_wait(&a_empty[js], aph ^ 1, abort, &g_td_err)) { ok = false; break; }
+        if (!mbar_wait_lim(&a_empty[js], aph ^ 1, abort, &g_td_err, p.wait_ns)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
         for (int q = 0; q < 3; ++q)
@@ -377,7 +378,7 @@ __global__ void __launch_bounds__(DTHREADS, 1)
     // red[q][m][n] (set js drains batch rows 8js .. 8js+7). The ring is free
     // once every MMA has completed (acc_full).
     float* red = reinterpret_cast<float*>(smem);
-    const bool have = ok && nsg > 0 && mbar_wait(&acc_full, 0, abort, &g_td_err);
+    const bool have = ok && nsg > 0 && mbar_wait_lim(&acc_full, 0, abort, &g_td_err, p.wait_ns);
     if (have) tc_fence_after();
     uint32_t r[3][8];
     if (have) {
@@ -503,7 +504,8 @@ TcDecodePlan plan_dec(int M, int N, int K, int dev) {
 template <int kBits>
 cudaError_t launch_dec(const __half* x, const uint32_t* const w[3], const __half* const s[3],
                        const float* scale, __half* const out[3], int M, int N, int K,
-                       const TcDecodePlan& pl, cudaStream_t stream) {
+                       const TcDecodePlan& pl, cudaStream_t stream,
+                       unsigned long long wait_ns = kWaitLimitNs) {
   using F = DFmt<kBits>;
   const int range = (pl.ng + pl.S - 1) / pl.S;
   const int sbox = kBits == 4 ? std::min(8, pl.ng) : 1;
@@ -520,6 +522,7 @@ cudaError_t launch_dec(const __half* x, const uint32_t* const w[3], const __half
   p.S = pl.S;
   p.ng = pl.ng;
   p.sbox = sbox;
+  p.wait_ns = wait_ns;
   const int nstg = (range + DGPS - 1) / DGPS;
   p.nst = std::min(std::min(nstg, DMAX_STAGES), (DSMEM_LIMIT - 1024 - sbytes) / F::kStage);
   p.nst = std::max(p.nst, 1);
@@ -577,6 +580,12 @@ cudaError_t launch_tc_decode(const __half* x, const uint32_t* const w[3], const 
                              __half* const out[3], int M, int N, int K, const TcDecodePlan& pl,
                              cudaStream_t stream) {
   return launch_dec<4>(x, w, s, nullptr, out, M, N, K, pl, stream);
+}
+
+cudaError_t launch_tc_decode_wait_limit(const __half* x, const uint32_t* const w[3], const __half* const s[3],
+                                        __half* const out[3], int M, int N, int K, const TcDecodePlan& pl,
+                                        unsigned long long wait_ns, cudaStream_t stream) {
+  return launch_dec<4>(x, w, s, nullptr, out, M, N, K, pl, stream, wait_ns);
 }
 
 cudaError_t launch_tc_decode_int8(const __half* x, const uint32_t* const w[3], const float scale[3],

@@ -31,6 +31,7 @@ _vp, _u32, _i32 = ctypes.c_void_p, ctypes.c_uint32, ctypes.c_int
 _SIGNATURES = {
     "kaio_qkv_project_int4": ([_vp] * 10 + [_u32, _u32, _u32, _vp], _i32),
     "kaio_qkv_project_int4_noalloc": ([_vp] * 10 + [_u32, _u32, _u32, _vp], _i32),
+    "kaio_debug_decode_wait_limit": ([_vp] * 10 + [_u32, _u32, _u32, ctypes.c_uint64, _vp], _i32),
     "kaio_matmul_tc": ([_vp, _vp, _vp, _u32, _u32, _u32, _vp], _i32),
     "kaio_matmul_tc_backward": ([_vp] * 5 + [_u32, _u32, _u32, _vp], _i32),
     "kaio_matmul_tc_f16": ([_vp, _vp, _vp, _u32, _u32, _u32, _vp], _i32),

@@ -214,3 +214,14 @@ def test_int8_binding_checks_shapes():
         kaio.qkv_project_int8(x, w, w, w, 1.0, 1.0, 1.0)
     with pytest.raises(ValueError):
         kaio.qkv_project_int8(torch.zeros(4, 100, dtype=torch.float16), w, w, w, 1.0, 1.0, 1.0)
+
+
+def test_wait_limit_entry_validates_before_touching_cuda(L):
+    p = [ptr(i) for i in range(10)]
+    assert L.kaio_debug_decode_wait_limit(*p, 17, 128, 256, 0, None) == INVALID   # decode shapes only
+    assert "1..16" in kaio.last_error()
+    assert L.kaio_debug_decode_wait_limit(*p, 4, 128, 200, 0, None) == INVALID   # K % 128
+    q = list(p)
+    q[3] = None
+    assert L.kaio_debug_decode_wait_limit(*q, 4, 128, 256, 0, None) == INVALID
+    assert "null" in kaio.last_error()
