@@ -277,7 +277,10 @@ def run_kaio(args, cfg_name, ws, rank, local, dist):
         for ws_ in weight_sets(N, K, nsets - 1, seed=1):
             sets.append(tuple(dev(a) for a in ws_))
         x = dev(inp.x)
-        outs = [torch.empty((M, N), dtype=torch.float16, device=device) for _ in range(3)]
+        # Q, K and V as three views of one [3, M, N] buffer, so that the e2e
+        # step reads the whole result back with one copy.
+        out_buf = torch.empty((3, M, N), dtype=torch.float16, device=device)
+        outs = [out_buf[j] for j in range(3)]
         lib = kaio.lib()
         ptr_sets = [[t.data_ptr() for t in s] for s in sets]
         xo = [x.data_ptr()] + [o.data_ptr() for o in outs]
@@ -291,7 +294,8 @@ def run_kaio(args, cfg_name, ws, rank, local, dist):
                 raise kaio.KaioError(st, kaio.last_error())
 
         def e2e_call(i, ins):
-            return kaio.qkv_project_int4(ins[0], *sets[i % len(sets)], out=outs, stream=stream)
+            kaio.qkv_project_int4(ins[0], *sets[i % len(sets)], out=outs, stream=stream)
+            return [out_buf]
         e2e_case = ([x], e2e_call, {"weights_resident": True})
 
         units_bytes = wbytes
@@ -309,7 +313,8 @@ def run_kaio(args, cfg_name, ws, rank, local, dist):
         for ws_ in weight_sets_int8(N, K, nsets - 1, seed=1):
             sets.append(tuple(dev(w) for w in ws_))
         x = dev(inp.x)
-        outs = [torch.empty((M, N), dtype=torch.float16, device=device) for _ in range(3)]
+        out_buf = torch.empty((3, M, N), dtype=torch.float16, device=device)
+        outs = [out_buf[j] for j in range(3)]
         lib = kaio.lib()
         ptr_sets = [[t.data_ptr() for t in s_] for s_ in sets]
         xo = [x.data_ptr()] + [o.data_ptr() for o in outs]
@@ -322,7 +327,8 @@ def run_kaio(args, cfg_name, ws, rank, local, dist):
                                                  xo[1], xo[2], xo[3], M, N, K, sp))
 
         def e2e_call(i, ins):
-            return kaio.qkv_project_int8(ins[0], *sets[i % len(sets)], *sc, out=outs, stream=stream)
+            kaio.qkv_project_int8(ins[0], *sets[i % len(sets)], *sc, out=outs, stream=stream)
+            return [out_buf]
         e2e_case = ([x], e2e_call, {"weights_resident": True})
 
         units_bytes = wbytes

@@ -10,6 +10,7 @@
 // "kaio-candle 0.2.0 -- src/matmul_tc_async.rs" (inner dimensions match, no CPU
 // fallback). Shapes are implied here by (M, N, K), so a row-count mismatch
 // cannot be expressed; what remains checkable is checked.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstdarg>
@@ -50,22 +51,34 @@ struct DeviceInfo {
 std::mutex g_mu;
 std::map<int, DeviceInfo> g_devices;
 
-// Current device; fills `info` (cached). Returns KAIO_OK or an error status.
+// Current device; fills `info` (cached, per host thread after the first
+// lookup). Returns KAIO_OK or an error status.
 int current_device(int* dev, DeviceInfo* info) {
   cudaError_t e = cudaGetDevice(dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-  std::lock_guard<std::mutex> lk(g_mu);
-  auto it = g_devices.find(*dev);
-  if (it == g_devices.end()) {
-    DeviceInfo d;
-    if ((e = cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, *dev)) != cudaSuccess ||
-        (e = cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, *dev)) != cudaSuccess ||
-        (e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, *dev)) != cudaSuccess)
-      return cuda_fail(e, "cudaDeviceGetAttribute");
-    d.ok = (d.major == 10 && d.minor == 3);
-    it = g_devices.emplace(*dev, d).first;
+  constexpr int kSlots = 64;
+  thread_local DeviceInfo slots[kSlots];
+  thread_local bool filled[kSlots] = {};
+  if (*dev >= 0 && *dev < kSlots && filled[*dev]) {
+    *info = slots[*dev];
+  } else {
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = g_devices.find(*dev);
+    if (it == g_devices.end()) {
+      DeviceInfo d;
+      if ((e = cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, *dev)) != cudaSuccess ||
+          (e = cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, *dev)) != cudaSuccess ||
+          (e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, *dev)) != cudaSuccess)
+        return cuda_fail(e, "cudaDeviceGetAttribute");
+      d.ok = (d.major == 10 && d.minor == 3);
+      it = g_devices.emplace(*dev, d).first;
+    }
+    *info = it->second;
+    if (*dev >= 0 && *dev < kSlots) {
+      slots[*dev] = *info;
+      filled[*dev] = true;
+    }
   }
-  *info = it->second;
   if (!info->ok)
     return fail(KAIO_ERR_UNSUPPORTED_DEVICE,
                 "device %d has compute capability %d.%d; this library is built for sm_103a "
@@ -73,6 +86,12 @@ int current_device(int* dev, DeviceInfo* info) {
                 *dev, info->major, info->minor);
   return KAIO_OK;
 }
+
+#define KAIO_TRY_FN(expr)        \
+  do {                           \
+    const int st__ = (expr);     \
+    if (st__ != KAIO_OK) return st__; \
+  } while (0)
 
 struct Span {
   const char* name;
@@ -112,22 +131,75 @@ int check_overlap(const Span* in, int n_in, const Span* out, int n_out) {
   return KAIO_OK;
 }
 
-// Each pointer must be device (or managed) memory of the current device.
+// Each pointer must be device (or managed) memory of the current device. One
+// driver query per allocation: it also returns the allocation's address
+// range, and a later tensor lying wholly inside a range already found to be
+// device memory of this device needs no query of its own (within this call;
+// nothing is remembered across calls, since memory may be freed in between).
+// Anything that is not plain device memory, or an unavailable driver entry
+// point, takes the runtime query and its messages.
+using PointerGetAttributesFn = CUresult (*)(unsigned int, CUpointer_attribute*, void**, CUdeviceptr);
+
+PointerGetAttributesFn pointer_attributes_fn() {
+  static PointerGetAttributesFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuPointerGetAttributes", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PointerGetAttributesFn>(f);
+  });
+  return fn;
+}
+
+int check_one_on_device(const Span& s, int dev) {
+  cudaPointerAttributes a{};
+  cudaError_t e = cudaPointerGetAttributes(&a, s.p);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(KAIO_ERR_INVALID_VALUE, "%s (%p) is not CUDA device memory (%s)", s.name, s.p,
+                cudaGetErrorName(e));
+  }
+  if (a.type != cudaMemoryTypeDevice && a.type != cudaMemoryTypeManaged)
+    return fail(KAIO_ERR_INVALID_VALUE, "%s (%p) is not device memory (memory type %d)", s.name, s.p,
+                static_cast<int>(a.type));
+  if (a.device != dev)
+    return fail(KAIO_ERR_INVALID_VALUE, "%s is on device %d but the current device is %d", s.name,
+                a.device, dev);
+  return KAIO_OK;
+}
+
 int check_on_device(const Span* s, int n, int dev) {
+  const PointerGetAttributesFn fn = pointer_attributes_fn();
+  constexpr int kMaxRanges = 16;
+  uintptr_t lo[kMaxRanges], hi[kMaxRanges];
+  int nr = 0;
   for (int i = 0; i < n; ++i) {
-    cudaPointerAttributes a{};
-    cudaError_t e = cudaPointerGetAttributes(&a, s[i].p);
-    if (e != cudaSuccess) {
-      cudaGetLastError();
-      return fail(KAIO_ERR_INVALID_VALUE, "%s (%p) is not CUDA device memory (%s)", s[i].name,
-                  s[i].p, cudaGetErrorName(e));
+    const uintptr_t p0 = reinterpret_cast<uintptr_t>(s[i].p), p1 = p0 + (s[i].bytes ? s[i].bytes : 1);
+    bool known = false;
+    for (int r = 0; r < nr && !known; ++r) known = p0 >= lo[r] && p1 <= hi[r];
+    if (known) continue;
+    if (fn) {
+      unsigned int mtype = 0;
+      int ordinal = -1;
+      CUdeviceptr start = 0;
+      size_t size = 0;
+      CUpointer_attribute attrs[4] = {CU_POINTER_ATTRIBUTE_MEMORY_TYPE, CU_POINTER_ATTRIBUTE_DEVICE_ORDINAL,
+                                      CU_POINTER_ATTRIBUTE_RANGE_START_ADDR, CU_POINTER_ATTRIBUTE_RANGE_SIZE};
+      void* data[4] = {&mtype, &ordinal, &start, &size};
+      if (fn(4, attrs, data, static_cast<CUdeviceptr>(p0)) == CUDA_SUCCESS &&
+          mtype == CU_MEMORYTYPE_DEVICE && ordinal == dev && size > 0) {
+        if (nr < kMaxRanges) {
+          lo[nr] = static_cast<uintptr_t>(start);
+          hi[nr] = static_cast<uintptr_t>(start) + size;
+          ++nr;
+        }
+        continue;
+      }
     }
-    if (a.type != cudaMemoryTypeDevice && a.type != cudaMemoryTypeManaged)
-      return fail(KAIO_ERR_INVALID_VALUE, "%s (%p) is not device memory (memory type %d)",
-                  s[i].name, s[i].p, static_cast<int>(a.type));
-    if (a.device != dev)
-      return fail(KAIO_ERR_INVALID_VALUE, "%s is on device %d but the current device is %d",
-                  s[i].name, a.device, dev);
+    KAIO_TRY_FN(check_one_on_device(s[i], dev));
   }
   return KAIO_OK;
 }

@@ -573,8 +573,30 @@ cudaError_t launch_dec(const __half* x, const uint32_t* const w[3], const __half
 
 }  // namespace
 
-TcDecodePlan plan_tc_decode(int M, int N, int K, int dev) { return plan_dec<4>(M, N, K, dev); }
-TcDecodePlan plan_tc_decode_int8(int M, int N, int K, int dev) { return plan_dec<8>(M, N, K, dev); }
+// The plan depends on (device, N, K, M <= 16) only; the last few are kept per
+// host thread, so a decode loop does not search cluster shapes on every call.
+template <int kBits>
+TcDecodePlan plan_dec_cached(int M, int N, int K, int dev) {
+  struct Entry {
+    int dev, N, K;
+    bool small;
+    TcDecodePlan pl;
+  };
+  thread_local Entry recent[8];
+  thread_local int n_recent = 0, next = 0;
+  const bool small = M <= DM;
+  for (int i = 0; i < n_recent; ++i)
+    if (recent[i].dev == dev && recent[i].N == N && recent[i].K == K && recent[i].small == small)
+      return recent[i].pl;
+  const TcDecodePlan pl = plan_dec<kBits>(M, N, K, dev);
+  recent[next] = Entry{dev, N, K, small, pl};
+  next = (next + 1) % 8;
+  if (n_recent < 8) ++n_recent;
+  return pl;
+}
+
+TcDecodePlan plan_tc_decode(int M, int N, int K, int dev) { return plan_dec_cached<4>(M, N, K, dev); }
+TcDecodePlan plan_tc_decode_int8(int M, int N, int K, int dev) { return plan_dec_cached<8>(M, N, K, dev); }
 
 cudaError_t launch_tc_decode(const __half* x, const uint32_t* const w[3], const __half* const s[3],
                              __half* const out[3], int M, int N, int K, const TcDecodePlan& pl,

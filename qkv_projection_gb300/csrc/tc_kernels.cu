@@ -33,6 +33,7 @@
 
 #include <map>
 #include <mutex>
+#include <unordered_map>
 #include <utility>
 
 #include "kaio_device.cuh"
@@ -583,6 +584,32 @@ __global__ void dequant_debug_kernel(const uint32_t* __restrict__ w, const __hal
 }  // namespace
 
 // ================================================================== host side
+namespace {
+// One encoded tensor map per distinct set of arguments, per host thread: a
+// map depends only on these values, and weights (and often activation
+// buffers) are the same from call to call. Encoding costs the calling thread
+// about as much as the rest of a decode call's host work together.
+struct TmKey {
+  uint64_t base, inner, outer, row_bytes;
+  uint32_t box_inner, box_outer, dtype, swz;
+  bool operator==(const TmKey& o) const {
+    return base == o.base && inner == o.inner && outer == o.outer && row_bytes == o.row_bytes &&
+           box_inner == o.box_inner && box_outer == o.box_outer && dtype == o.dtype && swz == o.swz;
+  }
+};
+struct TmKeyHash {
+  size_t operator()(const TmKey& k) const {
+    uint64_t h = k.base * 0x9E3779B97F4A7C15ull;
+    for (uint64_t v : {k.inner, k.outer, k.row_bytes,
+                       (static_cast<uint64_t>(k.box_inner) << 32) | k.box_outer,
+                       (static_cast<uint64_t>(k.dtype) << 32) | k.swz})
+      h = (h ^ v) * 0x100000001B3ull;
+    return static_cast<size_t>(h ^ (h >> 29));
+  }
+};
+constexpr size_t kTmCacheMax = 512;   // entries per host thread before the cache is emptied
+}  // namespace
+
 CUresult encode_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
                               uint64_t inner, uint64_t outer, uint64_t row_bytes,
                               uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swz) {
@@ -597,35 +624,59 @@ CUresult encode_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, const
       fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
   });
   if (!fn) return CUDA_ERROR_NOT_FOUND;
+  thread_local std::unordered_map<TmKey, CUtensorMap, TmKeyHash> cache;
+  const TmKey key{reinterpret_cast<uint64_t>(base), inner, outer, row_bytes, box_inner, box_outer,
+                  static_cast<uint32_t>(dtype), static_cast<uint32_t>(swz)};
+  auto it = cache.find(key);
+  if (it != cache.end()) {
+    *map = it->second;
+    return CUDA_SUCCESS;
+  }
   const cuuint64_t dims[2] = {inner, outer};
   const cuuint64_t strides[1] = {row_bytes};
   const cuuint32_t box[2] = {box_inner, box_outer};
   const cuuint32_t estr[2] = {1, 1};
-  return fn(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  const CUresult r = fn(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r == CUDA_SUCCESS) {
+    if (cache.size() >= kTmCacheMax) cache.clear();
+    cache.emplace(key, *map);
+  }
+  return r;
 }
 
 cudaError_t ensure_smem_limit(const void* kernel, int bytes) {
   // The attribute is one upper bound per (kernel, device): only ever raise it,
   // so that a launch needing less never lowers it under an earlier, larger need.
-  static std::mutex mu;
-  static std::map<std::pair<const void*, int>, int> limit;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  // A per-thread record of limits already in place spares the lock on every call.
+  thread_local std::map<std::pair<const void*, int>, int> seen;
+  auto hit = seen.find(std::make_pair(kernel, dev));
+  if (hit != seen.end() && bytes <= hit->second) return cudaSuccess;
+  static std::mutex mu;
+  static std::map<std::pair<const void*, int>, int> limit;
   std::lock_guard<std::mutex> lk(mu);
   int& cur = limit[std::make_pair(kernel, dev)];
-  if (bytes <= cur) return cudaSuccess;
+  if (bytes <= cur) {
+    seen[std::make_pair(kernel, dev)] = cur;
+    return cudaSuccess;
+  }
   cudaFuncAttributes fa{};
   e = cudaFuncGetAttributes(&fa, kernel);
   if (e != cudaSuccess) return e;
   if (fa.maxDynamicSharedSizeBytes >= bytes) {
     cur = fa.maxDynamicSharedSizeBytes;
+    seen[std::make_pair(kernel, dev)] = cur;
     return cudaSuccess;
   }
   e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (e == cudaSuccess) cur = bytes;
+  if (e == cudaSuccess) {
+    cur = bytes;
+    seen[std::make_pair(kernel, dev)] = cur;
+  }
   return e;
 }
 

@@ -121,12 +121,15 @@ def _need(t, name, dtypes, shape=None):
         raise ValueError(f"{name} has gradient tracking enabled; these ops are forward-only: detach() it")
 
 
+_PACKED = None
+
+
 def _packed_dtypes():
-    torch = _torch()
-    out = [torch.int32]
-    if hasattr(torch, "uint32"):
-        out.append(torch.uint32)
-    return tuple(out)
+    global _PACKED
+    if _PACKED is None:
+        torch = _torch()
+        _PACKED = (torch.int32, torch.uint32) if hasattr(torch, "uint32") else (torch.int32,)
+    return _PACKED
 
 
 # ------------------------------------------------------------------ public API
