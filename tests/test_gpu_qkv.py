@@ -200,3 +200,17 @@ def test_chained_calls_read_the_previous_calls_output():
     refs = oracle.qkv_project_int4_ref(q1_host, inp.wq, inp.wk, inp.wv, inp.sq, inp.sk, inp.sv)
     for o, r, name in zip((q2, k2, v2), refs, "QKV"):
         assert_qkv_close(to_host(o), r, f"chained {name}")
+
+
+@pytest.mark.parametrize("m", [1, 16, 64, 200])
+def test_mixed_scale_classes(m):
+    # Scales of every class in one problem, per lane and per group: a large
+    # scale at one column of group 1, negative scales over the second column
+    # tile, subnormal ones over the third, ordinary ones elsewhere.
+    n, k = 392, 512
+    inp = qkv_inputs(m, n, k, seed=m + 11)
+    for s in inp.scales():
+        s[1, 40] = np.float16(0.5)
+        s[:, 128:256] = -s[:, 128:256]
+        s[:, 256:384] = (s[:, 256:384].astype(np.float32) * np.float32(2.0 ** -12)).astype(np.float16)
+    check_full(inp, f"mixed scale classes M={m}")
