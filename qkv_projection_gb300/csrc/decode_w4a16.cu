@@ -258,10 +258,10 @@ DecodePlan plan_decode(int M, int N, int K, int num_sms) {
 // runtime's memory budget (inference engines and plugin hosts that hand out
 // every byte themselves and forbid cudaMalloc), processes whose device memory
 // is fully reserved up front, and real-time paths where an allocation's
-// implicit synchronisation or failure is not acceptable. For them the split-K
-// scratch of the decode kernel (per-group arrival counters and the partial
-// sums) lives in this fixed array instead of the workspace that
-// kaio_qkv_project_int4 allocates. Every GPU that loads the library holds
+// implicit synchronisation or failure is not acceptable. For them this
+// stream-K decode kernel, whose split-K needs global scratch (per-group
+// arrival counters and the partial sums), keeps that scratch in this fixed
+// array and allocates nothing. Every GPU that loads the library holds
 // these bytes until the process exits. All calls share the one array: calls
 // whose kernels overlap on the GPU (different streams, no ordering between
 // them) race on it and give wrong results; order them on one stream.

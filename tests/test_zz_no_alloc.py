@@ -2,8 +2,8 @@
 
 It serves callers that cannot allocate device memory (engines and plugin hosts
 that own all device memory, fully reserved processes, latency-critical paths):
-its split-K scratch is a fixed array inside the library instead of a workspace
-the library would otherwise need. Its results must match both the regular entry
+its stream-K kernel keeps its split-K scratch in a fixed array inside the
+library and allocates nothing. Its results must match both the regular entry
 point and the CPU oracle within the projection tolerance, element by element,
 on consecutive calls that share that array.
 
