@@ -568,6 +568,9 @@ def run_kaio(args, cfg_name, ws, rank, local, dist):
         "config": {"workload": cfg_name, **shape, "parallelism": f"replicas x{ws}", "l2": l2},
         "tflops": round(ws * flops / per_step_s / 1e12, 3) if kind not in DEQUANT_TYPES else None,
         "weight_gbs": round(ws * wbytes / per_step_s / 1e9, 3) if kind in ("qkv", "qkv8") else None,
+        # packed words alone (INT4: without the group scales; INT8 has no scale tensors)
+        "packed_weight_gbs": (round(ws * 3 * (shape["K"] * (4 if kind == "qkv" else 8) // 32) * shape["N"] * 4
+                                    / per_step_s / 1e9, 3) if kind in ("qkv", "qkv8") else None),
         "roofline": roof,
         "e2e": e2e,
         "gpu_launches": windows * steps * launches_per_step,
