@@ -293,10 +293,13 @@ def run_kaio(args, cfg_name, ws, rank, local, dist):
             if st:
                 raise kaio.KaioError(st, kaio.last_error())
 
-        def e2e_call(i, ins):
-            kaio.qkv_project_int4(ins[0], *sets[i % len(sets)], out=outs, stream=stream)
-            return [out_buf]
-        e2e_case = ([x], e2e_call, {"weights_resident": True})
+        def e2e_outs():
+            buf = torch.empty((3, M, N), dtype=torch.float16, device=device)
+            return [buf, [buf[j] for j in range(3)]]   # read back buf; the call writes its views
+
+        def e2e_call(i, ins, res):
+            kaio.qkv_project_int4(ins[0], *sets[i % len(sets)], out=res[1], stream=stream)
+        e2e_case = ([x], e2e_outs, e2e_call, {"weights_resident": True})
 
         units_bytes = wbytes
         alg_bytes = wbytes + obytes
@@ -326,10 +329,13 @@ def run_kaio(args, cfg_name, ws, rank, local, dist):
             kaio.check(lib.kaio_qkv_project_int8(xo[0], w[0], w[1], w[2], sc[0], sc[1], sc[2],
                                                  xo[1], xo[2], xo[3], M, N, K, sp))
 
-        def e2e_call(i, ins):
-            kaio.qkv_project_int8(ins[0], *sets[i % len(sets)], *sc, out=outs, stream=stream)
-            return [out_buf]
-        e2e_case = ([x], e2e_call, {"weights_resident": True})
+        def e2e_outs():
+            buf = torch.empty((3, M, N), dtype=torch.float16, device=device)
+            return [buf, [buf[j] for j in range(3)]]   # read back buf; the call writes its views
+
+        def e2e_call(i, ins, res):
+            kaio.qkv_project_int8(ins[0], *sets[i % len(sets)], *sc, out=res[1], stream=stream)
+        e2e_case = ([x], e2e_outs, e2e_call, {"weights_resident": True})
 
         units_bytes = wbytes
         alg_bytes = wbytes + obytes
@@ -366,11 +372,15 @@ def run_kaio(args, cfg_name, ws, rank, local, dist):
                 kaio.check(lib.kaio_dequantize_per_group(qcode, fcode, outer, axis, group, a.data_ptr(),
                                                          S.data_ptr(), o.data_ptr(), sp))
 
-        def e2e_call(i, ins):
+        def e2e_outs():
+            return [torch.empty_like(outs[0])]
+
+        def e2e_call(i, ins, res):
             if kind == "dqbwd":
-                return [kaio.dequantize_per_group_backward(ins[0], ins[1], group, out=outs[i % 2], stream=stream)]
-            return [kaio.dequantize_per_group(ins[0], ins[1], group, out=outs[i % 2], stream=stream)]
-        e2e_case = ([src, S], e2e_call, {})
+                kaio.dequantize_per_group_backward(ins[0], ins[1], group, out=res[0], stream=stream)
+            else:
+                kaio.dequantize_per_group(ins[0], ins[1], group, out=res[0], stream=stream)
+        e2e_case = ([src, S], e2e_outs, e2e_call, {})
 
         wbytes = 0
         units_bytes = dequant_bytes(kind, outer, axis, group)
@@ -396,10 +406,13 @@ def run_kaio(args, cfg_name, ws, rank, local, dist):
             kaio.check(bwd(A.data_ptr(), B.data_ptr(), G.data_ptr(), dA.data_ptr(), dB.data_ptr(),
                            M, N, K, sp))
 
-        def e2e_call(i, ins):
-            c = kaio.matmul_tc(ins[0], ins[1], out=C, stream=stream, out_dtype=out_t)
-            return [c, *kaio.matmul_tc_backward(ins[0], ins[1], ins[2], stream=stream, out_dtype=out_t)]
-        e2e_case = ([A, B, G], e2e_call, {})
+        def e2e_outs():
+            return [torch.empty_like(C), torch.empty_like(dA), torch.empty_like(dB)]
+
+        def e2e_call(i, ins, res):
+            kaio.matmul_tc(ins[0], ins[1], out=res[0], stream=stream, out_dtype=out_t)
+            kaio.matmul_tc_backward(ins[0], ins[1], ins[2], stream=stream, out_dtype=out_t, out=(res[1], res[2]))
+        e2e_case = ([A, B, G], e2e_outs, e2e_call, {})
 
         wbytes = 0
         units_bytes = 0
@@ -478,43 +491,80 @@ def run_kaio(args, cfg_name, ws, rank, local, dist):
                     "ms_per_step_max": round(win_ms[-1] / steps, 6)}
 
     # End to end through the public API: per step, copy the step's inputs in
-    # from pinned host memory, make the call(s), read every result back.
+    # from pinned host memory, make the call(s), read every result back into
+    # pinned host memory. Steps that move many bytes are pipelined the way a
+    # serving loop runs them: inputs in on one stream, the calls on the compute
+    # stream, results out on a third, with two sets of device buffers and
+    # events ordering each buffer's reuse, so step i's copies overlap steps
+    # i-1 and i+1. Small steps (decode) run in order on the compute stream:
+    # there the per-step host work of the extra streams and events costs more
+    # than the copies it would hide.
     e2e = None
     if not args.no_e2e:
-        dev_in, call, extra = e2e_case
+        dev_in, make_outs, call, extra = e2e_case
+        def tensors(res):
+            return [r for r in res if isinstance(r, torch.Tensor)]   # what a step reads back
+
+        step_bytes = sum(t.numel() * t.element_size() for t in dev_in) + \
+            sum(t.numel() * t.element_size() for t in tensors(make_outs()))
+        pipelined = step_bytes >= (16 << 20)
+        nb = 2 if pipelined else 1
         h_in = [t.cpu().pin_memory() for t in dev_in]
-        d_in = [torch.empty_like(t) for t in dev_in]
-        h_out = None
+        d_in = [[torch.empty_like(t) for t in dev_in] for _ in range(nb)]
+        d_out = [make_outs() for _ in range(nb)]
+        h_out = [[torch.empty(r.shape, dtype=r.dtype).pin_memory() for r in tensors(d_out[b])] for b in range(nb)]
+        r_out = [tensors(d_out[b]) for b in range(nb)]
+        s_in, s_out = (torch.cuda.Stream(device), torch.cuda.Stream(device)) if pipelined else (stream, stream)
+        ev_in = [torch.cuda.Event() for _ in range(nb)]
+        ev_comp = [torch.cuda.Event() for _ in range(nb)]
+        ev_out = [torch.cuda.Event() for _ in range(nb)]
         e_steps = max(args.steps, 200 if M <= 16 and kind in ("qkv", "qkv8") else 20)
         h2d = sum(t.numel() * t.element_size() for t in h_in)
 
         def e2e_step(i):
-            nonlocal h_out
-            for d, h in zip(d_in, h_in):
-                d.copy_(h, non_blocking=True)
-            res = call(i, d_in)
-            if h_out is None:
-                h_out = [torch.empty(r.shape, dtype=r.dtype).pin_memory() for r in res]
-            for h, r in zip(h_out, res):
-                h.copy_(r, non_blocking=True)
+            if not pipelined:                        # runs inside the compute stream's context
+                for d, h in zip(d_in[0], h_in):
+                    d.copy_(h, non_blocking=True)
+                call(i, d_in[0], d_out[0])
+                for h, r in zip(h_out[0], r_out[0]):
+                    h.copy_(r, non_blocking=True)
+                return
+            b = i % nb
+            s_in.wait_event(ev_comp[b])              # step i - nb has finished reading d_in[b]
+            with torch.cuda.stream(s_in):
+                for d, h in zip(d_in[b], h_in):
+                    d.copy_(h, non_blocking=True)
+                ev_in[b].record(s_in)
+            stream.wait_event(ev_in[b])
+            stream.wait_event(ev_out[b])             # step i - nb's results have left d_out[b]
+            with torch.cuda.stream(stream):
+                call(i, d_in[b], d_out[b])
+                ev_comp[b].record(stream)
+            s_out.wait_event(ev_comp[b])
+            with torch.cuda.stream(s_out):
+                for h, r in zip(h_out[b], r_out[b]):
+                    h.copy_(r, non_blocking=True)
+                ev_out[b].record(s_out)
 
         with torch.cuda.stream(stream):
             for i in range(3):
                 e2e_step(i)
-            stream.synchronize()
+            torch.cuda.synchronize(device)
             barrier(dist)
             t0 = time.perf_counter()
             for i in range(e_steps):
                 e2e_step(i)
-            stream.synchronize()
+            torch.cuda.synchronize(device)
             t1 = time.perf_counter()
         te = max_over_ranks(dist, t1 - t0, device)
-        d2h = sum(t.numel() * t.element_size() for t in h_out)
+        d2h = sum(t.numel() * t.element_size() for t in h_out[0])
         if kind in ("matmul", "matmul16") or bound == "tensor":
             e2e = {"value": round(ws * flops * e_steps / te / 1e12, 3), "unit": "TFLOP/s"}
         else:
             e2e = {"value": round(ws * units_bytes * e_steps / te / 1e9, 3), "unit": "GB/s"}
-        e2e.update({"h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e_steps, **extra})
+        e2e.update({"h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e_steps,
+                    "pipelining": "3 streams (in, compute, out), 2 buffer sets" if pipelined else "none (one stream)",
+                    **extra})
 
     if rank != 0:
         return None

@@ -209,9 +209,10 @@ def matmul_tc(a, b, out=None, stream=None, out_dtype=None):
     return out
 
 
-def matmul_tc_backward(a, b, g, stream=None, out_dtype=None):
+def matmul_tc_backward(a, b, g, stream=None, out_dtype=None, out=None):
     """(dA, dB) = (G @ B^T, A^T @ G) for C = A @ B, with g f16 [M, N]; the
-    results are f32 (default) or f16 (rounded in the kernels' epilogues)."""
+    results are f32 (default) or f16 (rounded in the kernels' epilogues),
+    written into ``out = (da, db)`` when given."""
     torch = _torch()
     _need(a, "a", (torch.float16,))
     _need(b, "b", (torch.float16,))
@@ -222,8 +223,13 @@ def matmul_tc_backward(a, b, g, stream=None, out_dtype=None):
     out_dtype = torch.float32 if out_dtype is None else out_dtype
     if out_dtype not in (torch.float32, torch.float16):
         raise ValueError(f"out_dtype must be float32 or float16, got {out_dtype}")
-    da = torch.empty((m, k), dtype=out_dtype, device=a.device)
-    db = torch.empty((k, n), dtype=out_dtype, device=a.device)
+    if out is None:
+        da = torch.empty((m, k), dtype=out_dtype, device=a.device)
+        db = torch.empty((k, n), dtype=out_dtype, device=a.device)
+    else:
+        da, db = out
+        _need(da, "da", (out_dtype,), (m, k))
+        _need(db, "db", (out_dtype,), (k, n))
     fn = lib().kaio_matmul_tc_backward if out_dtype == torch.float32 else lib().kaio_matmul_tc_backward_f16
     check(fn(a.data_ptr(), b.data_ptr(), g.data_ptr(), da.data_ptr(), db.data_ptr(), m, n, k,
              _stream_ptr(stream)))
