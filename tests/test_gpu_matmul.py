@@ -116,3 +116,17 @@ def test_f16_output_4096_sampled_rows():
     rows = np.unique(np.concatenate([np.random.default_rng(3).choice(4096, 48, replace=False),
                                      [0, 127, 128, 4095]]))
     assert rel_frobenius(c[rows].astype(np.float64), oracle.matmul_rows(a, b, rows)) <= TOL
+
+
+def test_backward_into_given_outputs():
+    import torch
+    a, b, g = dense_inputs(136, 264, 200, seed=11)
+    ad, bd, gd = to_dev(a), to_dev(b), to_dev(g)
+    da, db = kaio.matmul_tc_backward(ad, bd, gd)
+    oa = torch.full_like(da, float("nan"))
+    ob = torch.full_like(db, float("nan"))
+    ra, rb = kaio.matmul_tc_backward(ad, bd, gd, out=(oa, ob))
+    assert ra is oa and rb is ob
+    assert np.array_equal(to_host(oa), to_host(da)) and np.array_equal(to_host(ob), to_host(db))
+    with pytest.raises(ValueError):
+        kaio.matmul_tc_backward(ad, bd, gd, out=(ob, oa))   # shapes swapped
