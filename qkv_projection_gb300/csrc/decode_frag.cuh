@@ -1,6 +1,7 @@
-// Register-fragment building blocks shared by the two decode kernels
-// (weights streamed per k-block, dequantised straight into mma.sync A
-// fragments, x pre-permuted into B-fragment order in shared memory).
+// Register-fragment building blocks of the stream-K mma.sync decode kernel
+// behind the allocation-free entry (weights streamed per k-block, dequantised
+// straight into mma.sync A fragments, x pre-permuted into B-fragment order in
+// shared memory).
 //
 // Fragment mapping of one warp tile (32 output columns x one k-block of 64):
 // thread (g = lane/4, t = lane%4) holds packed rows 2t and 2t+1 of the k-block
