@@ -381,7 +381,7 @@ constexpr uint32_t kLoMask = 0x000F000Fu, kLoMagic = 0x64086408u;  // (lo, hi) b
 constexpr uint32_t kHiMask = 0x00F000F0u, kHiMagic = 0x54805480u;  // both bits 4..7
 constexpr uint32_t kMixMask = 0x00F0000Fu, kMixMagic = 0x54806408u; // lo bits 0..3, hi bits 20..23
 
-// "Paired" order, used by both decode kernels (tcgen05 and stream-K): pair j (0..3)
+// "Paired" order, used by the register-fragment decode path: pair j (0..3)
 // is the f16x2 {n_j, n_(j+4)} (low half = nibble j), scaled by s2 = {s, s}.
 // Costs one shift per word plus three ops per pair.
 struct PairedNibbles {
