@@ -46,27 +46,77 @@ __device__ unsigned g_tc_err = 0;
 namespace {
 
 // ============================================================== dense GEMM
-// A CTA pair computes a 256 x 256 tile of C with one tcgen05.mma of M = 256
-// per 16 K (cta_group::2): CTA rank r loads A rows m0 + 128r .. +127 and B
-// columns n0 + 128r .. +127 into its own shared memory and holds C rows
-// m0 + 128r .. +127 (all 256 columns) in its tensor memory. B is read once per
-// pair, and each SM's shared memory holds half of the B tile.
+// A CTA pair computes a 256-row tile of C with tcgen05.mma of M = 256 per 16 K
+// (cta_group::2): CTA rank r loads A rows m0 + 128r .. +127 into its own
+// shared memory and holds C rows m0 + 128r .. +127 in its tensor memory. Each
+// MMA has N = 256 columns, of which each CTA supplies 128 from its shared
+// memory, so every B column is read once per pair.
+//
+// Two tile widths (the host picks per call):
+//  * wide: 512 columns, two MMAs per 16 K into the CTA's whole 512-column
+//    TMEM. Each CTA takes 48 KB per 64-K step for 2 x 128 x 512 x 64 FLOPs,
+//    a quarter fewer bytes per FLOP than 256 columns; used when the wide tiles
+//    fill at least one wave of CTA pairs.
+//  * narrow: 256 columns, one MMA per 16 K into one of two 256-column TMEM
+//    buffers, so a tile's epilogue overlaps the next tile's main loop.
+// The epilogue stages each 128-byte-wide column chunk of the CTA's rows in
+// shared memory (128B-swizzled) and writes it with a TMA store; a wide tile's
+// TMEM is handed back as soon as its last chunk has been read, while the
+// stores drain on their own. (Row-per-thread global stores of the same data
+// cost a wide tile ~20 % of its time.)
 constexpr int GBM = 128;                       // rows of A (and of C) per CTA
-constexpr int GBN = 256;                       // columns of C per pair tile
-constexpr int GBK = 64, GSTAGES = 6;
+constexpr int GBK = 64;
 constexpr int GA_BYTES = GBM * GBK * 2;        // 16 KB
-constexpr int GB_BYTES = (GBN / 2) * GBK * 2;  // 16 KB: this CTA's half of B
-constexpr int GSTAGE_BYTES = GA_BYTES + GB_BYTES;
+constexpr int GB_PIECE = 128 * GBK * 2;        // 16 KB: 128 columns of B for one MMA
+constexpr int GMAX_STAGES = 6;
 constexpr int GTHREADS = 224;                  // w0, w6 TMA; w1 MMA (rank 0) + TMEM; w2..5 epilogue
-static_assert(GSTAGES % 2 == 0, "the two producers own alternate stages");
-constexpr uint32_t GTMEM_COLS = 512;           // 2 x 256 f32 accumulators
-constexpr size_t GSMEM = static_cast<size_t>(GSTAGES) * GSTAGE_BYTES + 1024;
+constexpr uint32_t GTMEM_COLS = 512;
+constexpr int GOUT_BUF = 128 * 128;            // one staged output chunk: 128 rows x 128 bytes
+constexpr size_t GSMEM = static_cast<size_t>(GMAX_STAGES) * (GA_BYTES + GB_PIECE) + 2 * GOUT_BUF + 1024;
+
+template <bool kWide>
+struct GShape {
+  static constexpr int kN = kWide ? 512 : 256;           // columns of C per pair tile
+  static constexpr int kPieces = kN / 256;                // MMAs per 16 K
+  static constexpr int kStageBytes = GA_BYTES + kPieces * GB_PIECE;
+  static constexpr int kStages = kWide ? 4 : 6;
+  static constexpr int kBufs = kWide ? 1 : 2;             // TMEM accumulators of kN columns
+  static_assert(kStages % 2 == 0, "the two producers own alternate stages");
+  static_assert(kStages * kStageBytes + 2 * GOUT_BUF + 1024 <= GSMEM, "shared memory");
+};
 
 struct GemmParams {
   void* c;              // f32 or f16 [M, N]
   int M, N, K;
-  int m_pairs, tiles;   // 256-row blocks; (256-row, 256-column) pair tiles
+  int m_pairs, tiles;   // 256-row blocks; pair tiles
 };
+
+// TMA store of one box from shared memory (bulk-group completion), and the
+// waits on this thread's outstanding bulk groups.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int c0, int c1) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(map),
+               "r"(smem_u32(src)), "r"(c0), "r"(c1)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// at most one group still reading its shared-memory source
+__device__ __forceinline__ void bulk_wait_read1() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+// every group complete (its writes performed)
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Named barrier that also ANDs a flag over its `count` threads, so that they
+// all take the same branch afterwards.
+__device__ __forceinline__ bool named_and(int id, int count, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %1, 0;\n\tbar.red.and.pred p, %2, %3, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(v)), "r"(id), "r"(count)
+      : "memory");
+  return r != 0;
+}
 
 // C16: the epilogue rounds the f32 accumulators to f16 (round-to-nearest-even)
 // and stores f16, fusing the cast the page's backward applies afterwards.
@@ -78,20 +128,23 @@ struct GemmParams {
 // 0's acc_empty. Persistent: pair p takes tiles p, p + pairs, ...; tiles are
 // numbered down the rows first, so the pairs running at one time share B tiles
 // through L2.
-template <bool A_MN, bool B_MN, bool C16>
+template <bool A_MN, bool B_MN, bool C16, bool kWide>
 __global__ void __launch_bounds__(GTHREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const GemmParams p) {
+                   const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
+  using S = GShape<kWide>;
+  constexpr int kStages = S::kStages, kStageBytes = S::kStageBytes;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = align_smem_1024(smem_raw);
-  __shared__ __align__(8) uint64_t full[GSTAGES], empty[GSTAGES], acc_full[2], acc_empty[2], mma_done;
+  unsigned char* out_stage = smem + kStages * kStageBytes;    // two 16 KB output chunks, 1024-aligned
+  __shared__ __align__(8) uint64_t full[kStages], empty[kStages], acc_full[2], acc_empty[2], mma_done;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rank = static_cast<int>(cluster_ctarank());
   if (threadIdx.x == 0) {
-    for (int s = 0; s < GSTAGES; ++s) {
+    for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);                  // rank 0's: its producer's expect_tx for both CTAs' bytes
       mbar_init(&empty[s], 1);                 // rank 0's MMA commit
     }
@@ -130,50 +183,54 @@ __global__ void __launch_bounds__(GTHREADS, 1)
       tma_prefetch_desc(&tmB);
       int st = 0;
       uint32_t ph = 0;
-      uint32_t fills[GSTAGES] = {};
+      uint32_t fills[kStages] = {};
       for (int t = pair; t < p.tiles; t += pstride) {
         const int m0 = (t % p.m_pairs) * (2 * GBM) + rank * GBM;
-        const int n0 = (t / p.m_pairs) * GBN + rank * (GBN / 2);
+        // this CTA's 128 columns of MMA j start at n0 + 256 j
+        const int n0 = (t / p.m_pairs) * S::kN + rank * 128;
         for (int kb = 0; kb < nk; ++kb) {
           if ((st & 1) != pid) {                 // the other producer's stage
-            if (++st == GSTAGES) { st = 0; ph ^= 1; }
+            if (++st == kStages) { st = 0; ph ^= 1; }
             continue;
           }
           if (!mbar_wait_cluster(&empty[st], ph ^ 1, abort, &g_tc_err)) goto producer_done;
           ++fills[st];
-          unsigned char* sa = smem + st * GSTAGE_BYTES;
+          unsigned char* sa = smem + st * kStageBytes;
           unsigned char* sb = sa + GA_BYTES;
           // Only rank 0's producer arrives (expecting both CTAs' bytes); rank
           // 1's copies count their bytes on rank 0's barrier directly. A
           // thread's arrive on another CTA's barrier stalls it for about as long
           // as a k-step takes, so no thread makes one per k-step.
           const uint32_t fb = at_rank0(&full[st]);
-          if (rank == 0) mbar_arrive_expect_tx(&full[st], 2 * GSTAGE_BYTES);
+          if (rank == 0) mbar_arrive_expect_tx(&full[st], 2 * kStageBytes);
           if (!A_MN) {
             tma_load_2d_pair(sa, &tmA, fb, kb * GBK, m0);
           } else {
             tma_load_2d_pair(sa, &tmA, fb, m0, kb * GBK);
             tma_load_2d_pair(sa + 8192, &tmA, fb, m0 + 64, kb * GBK);
           }
-          if (!B_MN) {
-            tma_load_2d_pair(sb, &tmB, fb, kb * GBK, n0);
-          } else {
-            tma_load_2d_pair(sb, &tmB, fb, n0, kb * GBK);
-            tma_load_2d_pair(sb + 8192, &tmB, fb, n0 + 64, kb * GBK);
+#pragma unroll
+          for (int j = 0; j < S::kPieces; ++j) {
+            if (!B_MN) {
+              tma_load_2d_pair(sb + j * GB_PIECE, &tmB, fb, kb * GBK, n0 + 256 * j);
+            } else {
+              tma_load_2d_pair(sb + j * GB_PIECE, &tmB, fb, n0 + 256 * j, kb * GBK);
+              tma_load_2d_pair(sb + j * GB_PIECE + 8192, &tmB, fb, n0 + 256 * j + 64, kb * GBK);
+            }
           }
-          if (++st == GSTAGES) { st = 0; ph ^= 1; }
+          if (++st == kStages) { st = 0; ph ^= 1; }
         }
       }
     producer_done:
       // No copy may still be landing in this CTA's shared memory when it
       // exits: every fill is consumed by an MMA (which waited for its bytes)
       // before its release reaches this CTA's stage.
-      for (int s2 = 0; s2 < GSTAGES; ++s2)
+      for (int s2 = 0; s2 < kStages; ++s2)
         if (fills[s2]) mbar_wait_cluster_drain(&empty[s2], (fills[s2] - 1) & 1, &g_tc_err);
     }
   } else if (warp == 1) {
     if (rank == 0 && lane == 0) {
-      constexpr uint32_t idesc = idesc_f16_f32(2 * GBM, GBN, A_MN, B_MN);
+      constexpr uint32_t idesc = idesc_f16_f32(2 * GBM, 256, A_MN, B_MN);
       int st = 0;
       uint32_t ph = 0;
       int buf = 0;
@@ -181,29 +238,33 @@ __global__ void __launch_bounds__(GTHREADS, 1)
       for (int t = pair; t < p.tiles; t += pstride) {
         if (!mbar_wait_cluster(&acc_empty[buf], aph ^ 1, abort, &g_tc_err)) break;
         tc_fence_after();
-        const uint32_t d = tmem + buf * GBN;
+        const uint32_t d = tmem + static_cast<uint32_t>(buf * S::kN);
         bool ok = true;
         for (int kb = 0; kb < nk; ++kb) {
           if (!mbar_wait_cluster(&full[st], ph, abort, &g_tc_err)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t sa = smem_u32(smem + st * GSTAGE_BYTES);
+          const uint32_t sa = smem_u32(smem + st * kStageBytes);
           const uint32_t sb = sa + GA_BYTES;
 #pragma unroll
           for (int kk = 0; kk < GBK / 16; ++kk) {
             const uint64_t ad = A_MN ? sdesc_sw128(sa + kk * 2048, 8192, 1024)
                                      : sdesc_sw128(sa + kk * 32, 16, 1024);
-            const uint64_t bd = B_MN ? sdesc_sw128(sb + kk * 2048, 8192, 1024)
-                                     : sdesc_sw128(sb + kk * 32, 16, 1024);
-            umma_ss_pair(d, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+#pragma unroll
+            for (int j = 0; j < S::kPieces; ++j) {
+              const uint32_t bj = sb + j * GB_PIECE;
+              const uint64_t bd = B_MN ? sdesc_sw128(bj + kk * 2048, 8192, 1024)
+                                       : sdesc_sw128(bj + kk * 32, 16, 1024);
+              umma_ss_pair(d + 256 * j, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+            }
           }
           umma_commit_pair(smem_u32(&empty[st]));
           umma_commit_pair(at_peer(&empty[st]));
-          if (++st == GSTAGES) { st = 0; ph ^= 1; }
+          if (++st == kStages) { st = 0; ph ^= 1; }
         }
         if (!ok) break;
         umma_commit_pair(smem_u32(&acc_full[buf]));
         umma_commit_pair(at_peer(&acc_full[buf]));
-        if (++buf == 2) { buf = 0; aph ^= 1; }
+        if (++buf == S::kBufs) { buf = 0; aph ^= 1; }
       }
       // Every MMA issued (and with it every commit to either CTA) has
       // completed before TMEM is released.
@@ -211,48 +272,76 @@ __global__ void __launch_bounds__(GTHREADS, 1)
       mbar_wait_cluster_drain(&mma_done, 0, &g_tc_err);
     }
   } else if (warp <= 5) {
-    // Epilogue: warp w drains TMEM lanes 32*(w%4) .. +31 (rows of this CTA's half).
+    // Epilogue: warp w drains TMEM lanes 32*(w%4) .. +31 (this CTA's rows) in
+    // chunks of 128 bytes per row (32 f32 or 64 f16 columns): TMEM ->
+    // registers -> a 128B-swizzled 16 KB staging buffer (two, alternating) ->
+    // one TMA store per chunk, issued by warp 2's lane 0 once all four warps
+    // have written it. TMA clips rows >= M and columns >= N.
+    constexpr int kChunkCols = C16 ? 64 : 32;
+    constexpr int kChunks = S::kN / kChunkCols;
+    const bool issuer = warp == 2 && lane == 0;
     const int sp = warp & 3;
-    int buf = 0;
+    const int row = 32 * sp + lane;             // row of the CTA's 128 in the chunk
+    const uint32_t row_tmem = static_cast<uint32_t>(32 * sp) << 16;
+    int buf = 0, ob = 0, nstored = 0;
     uint32_t aph = 0;
     for (int t = pair; t < p.tiles; t += pstride) {
-      const int m0 = (t % p.m_pairs) * (2 * GBM) + rank * GBM, n0 = (t / p.m_pairs) * GBN;
-      if (!mbar_wait_cluster(&acc_full[buf], aph, abort, &g_tc_err)) break;
+      const int m0 = (t % p.m_pairs) * (2 * GBM) + rank * GBM, n0 = (t / p.m_pairs) * S::kN;
+      // the four warps meet at named barriers below: they leave together
+      const bool got = mbar_wait_cluster(&acc_full[buf], aph, abort, &g_tc_err);
+      if (!named_and(1, 128, got)) break;
       tc_fence_after();
-      const int row = m0 + 32 * sp + lane;
 #pragma unroll 1
-      for (int ch = 0; ch < GBN / 32; ++ch) {
-        uint32_t r[32];
-        tmem_ld32(tmem + (static_cast<uint32_t>(32 * sp) << 16) + buf * GBN + ch * 32, r);
-        tmem_ld_wait();
-        const int col0 = n0 + ch * 32;
-        if (row < p.M) {
+      for (int ch = 0; ch < kChunks; ++ch) {
+        uint32_t r[kChunkCols];
+        if constexpr (C16) {
+          uint32_t lo[32], hi[32];
+          tmem_ld32(tmem + row_tmem + buf * S::kN + ch * 64, lo);
+          tmem_ld32(tmem + row_tmem + buf * S::kN + ch * 64 + 32, hi);
+          tmem_ld_wait();
 #pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const int col = col0 + 4 * q;
-            if (col >= p.N) continue;
-            if (C16) {
-              __half* crow = static_cast<__half*>(p.c) + static_cast<size_t>(row) * p.N;
-              const __half2 lo = __floats2half2_rn(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]));
-              const __half2 hi = __floats2half2_rn(__uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
-              uint2 u;
-              u.x = *reinterpret_cast<const uint32_t*>(&lo);
-              u.y = *reinterpret_cast<const uint32_t*>(&hi);
-              *reinterpret_cast<uint2*>(crow + col) = u;
-            } else {
-              float* crow = static_cast<float*>(p.c) + static_cast<size_t>(row) * p.N;
-              *reinterpret_cast<float4*>(crow + col) =
-                  make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
-                              __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
-            }
+          for (int i = 0; i < 16; ++i) {
+            const __half2 a2 = __floats2half2_rn(__uint_as_float(lo[2 * i]), __uint_as_float(lo[2 * i + 1]));
+            const __half2 b2 = __floats2half2_rn(__uint_as_float(hi[2 * i]), __uint_as_float(hi[2 * i + 1]));
+            r[i] = *reinterpret_cast<const uint32_t*>(&a2);
+            r[16 + i] = *reinterpret_cast<const uint32_t*>(&b2);
           }
+        } else {
+          tmem_ld32(tmem + row_tmem + buf * S::kN + ch * 32, r);
+          tmem_ld_wait();
         }
+        if (ch == kChunks - 1) {
+          // the whole accumulator has been read: hand it back to the MMAs
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(at_rank0(&acc_empty[buf]));
+        }
+        // staging buffer ob is free once the store issued from it two chunks
+        // ago has read it
+        if (issuer && nstored >= 2) bulk_wait_read1();
+        named_sync(1, 128);
+        unsigned char* dst = out_stage + ob * GOUT_BUF + row * 128;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const uint4 v = make_uint4(r[4 * u], r[4 * u + 1], r[4 * u + 2], r[4 * u + 3]);
+          *reinterpret_cast<uint4*>(dst + ((u ^ (row & 7)) << 4)) = v;
+        }
+        fence_proxy_async_smem();
+        named_sync(1, 128);
+        if (issuer) {
+          // a box wholly outside C writes nothing; its group is committed
+          // (empty) all the same, so that the group two back is always the
+          // store that last read this staging buffer
+          if (m0 < p.M && n0 + ch * kChunkCols < p.N)
+            tma_store_2d(&tmC, out_stage + ob * GOUT_BUF, n0 + ch * kChunkCols, m0);
+          bulk_commit();
+        }
+        ++nstored;
+        ob ^= 1;
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(at_rank0(&acc_empty[buf]));
-      if (++buf == 2) { buf = 0; aph ^= 1; }
+      if (++buf == S::kBufs) { buf = 0; aph ^= 1; }
     }
+    if (issuer) bulk_wait_all();                // every store done before the CTA exits
   }
 
   tc_fence_before();
@@ -749,14 +838,23 @@ cudaError_t launch_tc_gemm(const void* a, const void* b, void* c, GemmShape sh, 
                              static_cast<uint64_t>(sh.M) * 2, 64, GBK, CU_TENSOR_MAP_SWIZZLE_128B);
   if (r != CUDA_SUCCESS) return map_error(r);
   // Bop is [K x N]; stored [N][K] (K-major) or [K][N] (MN-major). Each CTA of
-  // a pair loads its 128 columns: one 128-row K-major box, or two 64-column
-  // MN-major boxes.
+  // a pair loads 128 columns per MMA: one 128-row K-major box, or two
+  // 64-column MN-major boxes.
   if (!b_mn)
     r = encode_tensor_map_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, b, sh.K, sh.N,
-                             static_cast<uint64_t>(sh.K) * 2, GBK, GBN / 2, CU_TENSOR_MAP_SWIZZLE_128B);
+                             static_cast<uint64_t>(sh.K) * 2, GBK, 128, CU_TENSOR_MAP_SWIZZLE_128B);
   else
     r = encode_tensor_map_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, b, sh.N, sh.K,
                              static_cast<uint64_t>(sh.N) * 2, 64, GBK, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (r != CUDA_SUCCESS) return map_error(r);
+  // C [M][N] f32 or f16, stored by the epilogue in 128-row x 128-byte boxes.
+  CUtensorMap tc;
+  if (c_f16)
+    r = encode_tensor_map_2d(&tc, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, c, sh.N, sh.M,
+                             static_cast<uint64_t>(sh.N) * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+  else
+    r = encode_tensor_map_2d(&tc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, c, sh.N, sh.M,
+                             static_cast<uint64_t>(sh.N) * 4, 32, 128, CU_TENSOR_MAP_SWIZZLE_128B);
   if (r != CUDA_SUCCESS) return map_error(r);
 
   GemmParams p{};
@@ -765,28 +863,45 @@ cudaError_t launch_tc_gemm(const void* a, const void* b, void* c, GemmShape sh, 
   p.N = sh.N;
   p.K = sh.K;
   p.m_pairs = (sh.M + 2 * GBM - 1) / (2 * GBM);
-  const int n_blocks = (sh.N + GBN - 1) / GBN;
-  p.tiles = p.m_pairs * n_blocks;
 
-  cudaError_t e;
-  const void* kern = nullptr;
-#define KAIO_PICK_GEMM(AM, BM_)                                                                         \
-  kern = c_f16 ? reinterpret_cast<const void*>(tc_gemm_kernel<AM, BM_, true>)                           \
-               : reinterpret_cast<const void*>(tc_gemm_kernel<AM, BM_, false>)
-  if (!a_mn && b_mn) KAIO_PICK_GEMM(false, true);
-  else if (!a_mn && !b_mn) KAIO_PICK_GEMM(false, false);
-  else if (a_mn && b_mn) KAIO_PICK_GEMM(true, true);
-  else KAIO_PICK_GEMM(true, false);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  auto pick = [&](bool wide) -> const void* {
+#define KAIO_PICK_GEMM(AM, BM_, W)                                                                      \
+  return c_f16 ? reinterpret_cast<const void*>(tc_gemm_kernel<AM, BM_, true, W>)                        \
+               : reinterpret_cast<const void*>(tc_gemm_kernel<AM, BM_, false, W>)
+    if (wide) {
+      if (!a_mn && b_mn) KAIO_PICK_GEMM(false, true, true);
+      if (!a_mn && !b_mn) KAIO_PICK_GEMM(false, false, true);
+      if (a_mn && b_mn) KAIO_PICK_GEMM(true, true, true);
+      KAIO_PICK_GEMM(true, false, true);
+    }
+    if (!a_mn && b_mn) KAIO_PICK_GEMM(false, true, false);
+    if (!a_mn && !b_mn) KAIO_PICK_GEMM(false, false, false);
+    if (a_mn && b_mn) KAIO_PICK_GEMM(true, true, false);
+    KAIO_PICK_GEMM(true, false, false);
 #undef KAIO_PICK_GEMM
+  };
+  // Wide (512-column) tiles when they fill at least one wave of resident CTA
+  // pairs (a pair sits in one GPC); narrow ones otherwise, so that small
+  // problems spread over more SMs.
+  const void* kern = pick(true);
+  int slots = gemm_max_active_pairs(kern, dev);
+  if (slots <= 0) slots = num_sms / 2;
+  const int wide_tiles = p.m_pairs * ((sh.N + 511) / 512);
+  const bool wide = wide_tiles >= slots;
+  if (!wide) {
+    kern = pick(false);
+    const int s2 = gemm_max_active_pairs(kern, dev);
+    if (s2 > 0) slots = s2;
+  }
+  p.tiles = wide ? wide_tiles : p.m_pairs * ((sh.N + 255) / 256);
   e = ensure_smem_limit(kern, static_cast<int>(GSMEM));
   if (e != cudaSuccess) return e;
-  // Persistent: as many CTA pairs as can be resident at once (a pair sits in
-  // one GPC), capped by the number of tiles.
-  int dev = 0;
-  e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  const int slots = gemm_max_active_pairs(kern, dev);
-  const int pairs = std::max(1, std::min(p.tiles, slots > 0 ? slots : num_sms / 2));
+  // Persistent: as many CTA pairs as can be resident at once, capped by the
+  // number of tiles.
+  const int pairs = std::max(1, std::min(p.tiles, slots));
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
   cfg.blockDim = dim3(GTHREADS);
@@ -799,7 +914,7 @@ cudaError_t launch_tc_gemm(const void* a, const void* b, void* c, GemmShape sh, 
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  void* args[] = {&ta, &tb, &p};
+  void* args[] = {&ta, &tb, &tc, &p};
   e = cudaLaunchKernelExC(&cfg, kern, args);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
