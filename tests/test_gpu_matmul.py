@@ -130,3 +130,20 @@ def test_backward_into_given_outputs():
     assert np.array_equal(to_host(oa), to_host(da)) and np.array_equal(to_host(ob), to_host(db))
     with pytest.raises(ValueError):
         kaio.matmul_tc_backward(ad, bd, gd, out=(ob, oa))   # shapes swapped
+
+
+# Wide (512-column) pair tiles are used when they fill a wave of resident CTA
+# pairs: (2432, 4232, 64) gives 10 x 9 = 90 of them, with a half-empty last
+# pair of row blocks and a last column block 136 wide, whose chunks beyond N
+# the epilogue skips.
+def test_forward_wide_tiles_ragged_edges():
+    import torch
+    a, b, _ = dense_inputs(2432, 4232, 64, seed=5)
+    ad, bd = to_dev(a), to_dev(b)
+    c = to_host(kaio.matmul_tc(ad, bd))
+    ref = oracle.matmul_ref(a, b)
+    assert rel_frobenius(c, ref) <= TOL
+    assert rel_frobenius(c[:, 4096:], ref[:, 4096:]) <= TOL      # the ragged column block
+    assert rel_frobenius(c[2304:], ref[2304:]) <= TOL            # the half-empty row pair
+    c16 = to_host(kaio.matmul_tc(ad, bd, out_dtype=torch.float16))
+    assert np.array_equal(c16.view(np.uint16), c.astype(np.float16).view(np.uint16))
