@@ -214,3 +214,11 @@ def test_mixed_scale_classes(m):
         s[:, 128:256] = -s[:, 128:256]
         s[:, 256:384] = (s[:, 256:384].astype(np.float32) * np.float32(2.0 ** -12)).astype(np.float16)
     check_full(inp, f"mixed scale classes M={m}")
+
+
+@pytest.mark.parametrize("m", [2, 5, 11])
+def test_decode_rows_not_a_multiple_of_the_cluster(m):
+    # The cluster's ranks finish batch rows m = rank, rank + S, ...: with M not a
+    # multiple of S some ranks finish fewer rows than others (here K = 8192 over
+    # 64 groups and a ragged last column tile).
+    check_full(qkv_inputs(m, 1032, 8192, seed=100 + m), f"M={m} N=1032 K=8192")
