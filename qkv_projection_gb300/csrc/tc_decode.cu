@@ -48,6 +48,7 @@ constexpr int DGPS = 2;                          // K groups (of 128 K) per shar
 constexpr int DXBOX = DM * 64 * 2;               // one 64-K x box, 16 rows, 128B-swizzled: 2 KB
 constexpr int DX_STAGE = DGPS * 2 * DXBOX;       // 8 KB
 constexpr int DMAX_STAGES = 4;
+constexpr int DMAX_X = 8;                        // INT8: x ring slots (one stage's x boxes each)
 constexpr int DSCALE_ROW = 3 * DN * 2;           // the three scale rows of one K group: 768 B
 constexpr int DDQ_WARPS = 8;                     // 2 per TMEM lane quadrant
 constexpr int DMMA_WARPS = 3;                    // one per projection
@@ -63,11 +64,21 @@ static_assert(DA_COL0 + DASTAGES * DA_STAGE_COLS <= DTMEM_COLS, "TMEM layout");
 
 // Stage layout of one weight format (kBits = 4: INT4 with f16 group scales;
 // kBits = 8: INT8 with one f32 scale per projection, applied in the epilogue).
+//
+// INT8 keeps its x boxes in a ring of their own (kSplitX): a weight stage is
+// refilled as soon as its words are in the conversion warps' registers, while
+// the x boxes stay until the MMAs reading them are done. Its 96 KB weight
+// stages are few (two fit), and this freed them ~10 % sooner at M = 16,
+// K = N = 8192 (38.4 -> 35.0 us). INT4 (48 KB of words per stage, x permuted
+// in place by the dequant warps) measured slower that way (30.1 -> 32.4 us)
+// and keeps x and words in one stage.
 template <int kBits>
 struct DFmt {
+  static constexpr bool kSplitX = kBits == 8;
   static constexpr int kRows = 128 * kBits / 32;        // packed rows per K group: 16 or 32
   static constexpr int kWBox = DGPS * kRows * DN * 4;   // one projection's words per stage: 16 or 32 KB
-  static constexpr int kStage = DX_STAGE + 3 * kWBox;   // 56 or 104 KB
+  static constexpr int kXIn = kSplitX ? 0 : DX_STAGE;   // x bytes inside a stage (before the words)
+  static constexpr int kStage = kXIn + 3 * kWBox;       // 56 KB (x + words) or 96 KB (words)
   static_assert(kStage % 1024 == 0, "x boxes stay 1024-aligned");
   static_assert(DRED_BYTES <= kStage, "partials reuse the ring");
 };
@@ -80,7 +91,9 @@ struct DecTcParams {
   int S;         // cluster size: K ranges per column tile
   int ng;        // K / 128
   int nst;       // ring stages (DGPS K groups each)
-  int s_off;     // byte offset of the scale rows (after the ring)
+  int nx;        // INT8: x ring slots (one stage's x boxes each)
+  int x_off;     // INT8: byte offset of the x ring (after the stage ring)
+  int s_off;     // byte offset of the scale rows (after the rings)
   int sbox;      // scale rows per TMA box
   unsigned long long wait_ns;   // limit of every pipeline wait (kWaitLimitNs; shorter in a test)
 };
@@ -95,8 +108,8 @@ __global__ void __launch_bounds__(DTHREADS, 1)
   constexpr int DW_BOX = F::kWBox, DSTAGE_BYTES = F::kStage;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = align_smem_1024(smem_raw);
-  __shared__ __align__(8) uint64_t full[DMAX_STAGES], empty[DMAX_STAGES], sbar0, sbar, a_full[DASTAGES],
-      a_empty[DASTAGES], acc_full, mma_done[DMMA_WARPS];
+  __shared__ __align__(8) uint64_t full[DMAX_STAGES], empty[DMAX_STAGES], xfull[DMAX_X], xempty[DMAX_X], sbar0,
+      sbar, a_full[DASTAGES], a_empty[DASTAGES], acc_full, mma_done[DMMA_WARPS];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
 
@@ -116,23 +129,37 @@ __global__ void __launch_bounds__(DTHREADS, 1)
   // once stage 0 has landed (every SM asks for its first stages at the same
   // moment, and copies issued together land together).
   uint32_t fills[DMAX_STAGES] = {0, 0, 0, 0};
-  int pst = 0, pi = 0;
+  uint32_t xfills[DMAX_X] = {};
+  int pst = 0, pi = 0, xi = 0;
   uint32_t pph = 0;
   const int nsb = kBits == 4 ? (nsg + p.sbox - 1) / p.sbox : 0;   // boxes of scale rows
   auto issue_stage = [&]() {
     unsigned char* sx = smem + pst * DSTAGE_BYTES;
-    unsigned char* sw = sx + DX_STAGE;
+    unsigned char* sw = sx + F::kXIn;
     const int g = g_begin + pi * DGPS;
     mbar_arrive_expect_tx(&full[pst], DSTAGE_BYTES);
     tma_load_2d(sw, &tmW0, &full[pst], n0, g * F::kRows);
     tma_load_2d(sw + DW_BOX, &tmW1, &full[pst], n0, g * F::kRows);
     tma_load_2d(sw + 2 * DW_BOX, &tmW2, &full[pst], n0, g * F::kRows);
+    if constexpr (!F::kSplitX) {
 #pragma unroll
-    for (int b = 0; b < 2 * DGPS; ++b)
-      tma_load_2d(sx + b * DXBOX, &tmX, &full[pst], (g * 2 + b) * 64, 0);
+      for (int b = 0; b < 2 * DGPS; ++b)
+        tma_load_2d(sx + b * DXBOX, &tmX, &full[pst], (g * 2 + b) * 64, 0);
+    }
     ++fills[pst];
     ++pi;
     if (++pst == p.nst) { pst = 0; pph ^= 1; }
+  };
+  auto issue_x = [&]() {                          // INT8: stage xi's x boxes into the x ring
+    const int xs = xi % p.nx;
+    unsigned char* sx = smem + p.x_off + xs * DX_STAGE;
+    const int g = g_begin + xi * DGPS;
+    mbar_arrive_expect_tx(&xfull[xs], DX_STAGE);
+#pragma unroll
+    for (int b = 0; b < 2 * DGPS; ++b)
+      tma_load_2d(sx + b * DXBOX, &tmX, &xfull[xs], (g * 2 + b) * 64, 0);
+    ++xfills[xs];
+    ++xi;
   };
   auto issue_scales = [&](int b, uint64_t* bar) {
     unsigned char* ss = smem + p.s_off + b * p.sbox * DSCALE_ROW;
@@ -144,7 +171,14 @@ __global__ void __launch_bounds__(DTHREADS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.nst; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], DDQ_WARPS + DMMA_WARPS);   // dequant warps + one commit per MMA warp
+      // dequant warps (+ one commit per MMA warp when the stage holds x)
+      mbar_init(&empty[s], DDQ_WARPS + (F::kSplitX ? 0 : DMMA_WARPS));
+    }
+    if constexpr (F::kSplitX) {
+      for (int s = 0; s < p.nx; ++s) {
+        mbar_init(&xfull[s], 1);
+        mbar_init(&xempty[s], DMMA_WARPS);            // one commit per MMA warp
+      }
     }
     mbar_init(&sbar0, 1);
     mbar_init(&sbar, 1);
@@ -172,12 +206,18 @@ __global__ void __launch_bounds__(DTHREADS, 1)
       tma_prefetch_l2_2d(&tmW2, n0, g_begin * F::kRows);
     }
     grid_dependency_wait();                       // the previous kernel's writes are visible
-    if (nstg > 0) issue_stage();
+    if (nstg > 0) {
+      issue_stage();
+      if constexpr (F::kSplitX) issue_x();
+    }
     if (nsb > 0) {
       mbar_arrive_expect_tx(&sbar0, static_cast<uint32_t>(3 * p.sbox * DN * 2));
       issue_scales(0, &sbar0);
     }
-    if (pi < nstg && pi < p.nst) issue_stage();
+    if (pi < nstg && pi < p.nst) {
+      issue_stage();
+      if constexpr (F::kSplitX) issue_x();
+    }
     if (nsb > 1) {
       mbar_arrive_expect_tx(&sbar, static_cast<uint32_t>(3 * (nsb - 1) * p.sbox * DN * 2));
       for (int b = 1; b < nsb; ++b) issue_scales(b, &sbar);
@@ -201,10 +241,31 @@ __global__ void __launch_bounds__(DTHREADS, 1)
     // with the first two stages).
     if (lane == 0) {
       bool ok = pi >= nstg || pi >= p.nst || mbar_wait_lim(&full[0], 0, abort, &g_td_err, p.wait_ns);
-      while (ok && pi < nstg && pi < p.nst) issue_stage();   // the rest of the first ring
+      while (ok && pi < nstg && pi < p.nst) issue_stage();   // the rest of the first ring(s)
+      if constexpr (F::kSplitX)
+        while (ok && xi < nstg && xi < p.nx) issue_x();
       while (ok && pi < nstg) {
         if (!mbar_wait_lim(&empty[pst], pph ^ 1, abort, &g_td_err, p.wait_ns)) break;
         issue_stage();
+        if constexpr (F::kSplitX) {
+          // x of stage xi reuses the slot of stage xi - nx (nx >= nst: its
+          // MMAs finished long before)
+          while (ok && xi < pi && xi < nstg) {
+            if (!mbar_wait_lim(&xempty[xi % p.nx], ((xi / p.nx) - 1) & 1, abort, &g_td_err, p.wait_ns)) {
+              ok = false;
+              break;
+            }
+            issue_x();
+          }
+        }
+      }
+      if constexpr (F::kSplitX) {
+        while (ok && xi < nstg) {
+          if (!mbar_wait_lim(&xempty[xi % p.nx], ((xi / p.nx) - 1) & 1, abort, &g_td_err, p.wait_ns)) break;
+          issue_x();
+        }
+        for (int s2 = 0; s2 < p.nx; ++s2)
+          if (xfills[s2]) mbar_wait_drain(&xfull[s2], (xfills[s2] - 1) & 1, &g_td_err);
       }
       for (int s2 = 0; s2 < p.nst; ++s2)
         if (fills[s2]) mbar_wait_drain(&full[s2], (fills[s2] - 1) & 1, &g_td_err);
@@ -226,7 +287,8 @@ __global__ void __launch_bounds__(DTHREADS, 1)
     uint32_t aph = 0;
     bool ok = true;
     for (int i = 0; i < nstg && ok; ++i) {
-      unsigned char* sx = smem + st * DSTAGE_BYTES;
+      const int xs = i % p.nx;
+      unsigned char* sx = F::kSplitX ? smem + p.x_off + xs * DX_STAGE : smem + st * DSTAGE_BYTES;
       const uint64_t bd0 = sdesc_sw128(smem_u32(sx), 16, 1024);
       const uint32_t blo = static_cast<uint32_t>(bd0), bhi = static_cast<uint32_t>(bd0 >> 32);
       const int ngs = min(DGPS, nsg - i * DGPS);
@@ -247,7 +309,7 @@ __global__ void __launch_bounds__(DTHREADS, 1)
               umma_ts_lohi(dq, abase + (kBits == 4 ? kk * 16 + hh * 8 : hh * 32 + kk * 8),
                            xlo + ((hh * DXBOX + kk * 32) >> 4), bhi, idesc, (hh | kk) != 0 ? 1u : acc0);
           umma_commit(&a_empty[a]);
-          if (j == ngs - 1) umma_commit(&empty[st]);
+          if (j == ngs - 1) umma_commit(F::kSplitX ? &xempty[xs] : &empty[st]);
         }
         __syncwarp();
         if (++a == DASTAGES) { a = 0; aph ^= 1; }
@@ -294,12 +356,19 @@ __global__ void __launch_bounds__(DTHREADS, 1)
           fence_proxy_async_smem();               // the MMAs read x through the async proxy
         }
         if constexpr (kBits == 8) {
+          // The stage's x boxes (own ring) have landed before this set hands
+          // its A stage to the MMAs that read them.
+          if (!mbar_wait_lim(&xfull[i % p.nx], static_cast<uint32_t>(i / p.nx) & 1u, abort, &g_td_err,
+                             p.wait_ns)) {
+            ok = false;
+            break;
+          }
           // Thread = column nl: its 32 packed rows of the group per projection,
           // converted exactly to f16 K pairs. Column c of projection q's 64 holds
           // K pair c (K-rows 2c, 2c+1: byte pair c % 2 of packed row c / 2).
           if (!mbar_wait_lim(&a_empty[js], aph ^ 1, abort, &g_td_err, p.wait_ns)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t* sw = reinterpret_cast<const uint32_t*>(smem + st * DSTAGE_BYTES + DX_STAGE) +
+          const uint32_t* sw = reinterpret_cast<const uint32_t*>(smem + st * DSTAGE_BYTES + F::kXIn) +
                                js * F::kRows * DN + nl;
 #pragma unroll
           for (int q = 0; q < 3; ++q)
@@ -328,7 +397,7 @@ __global__ void __launch_bounds__(DTHREADS, 1)
         }
         // scale rows of group gl: box gl/8 (boxes hold up to 8 rows), row gl%8
         const unsigned char* sc = scale_base + (gl >> 3) * p.sbox * DSCALE_ROW + (gl & 7) * (DN * 2);
-        const unsigned char* sw = smem + st * DSTAGE_BYTES + DX_STAGE + js * 16 * (DN * 4) + nl * 4;
+        const unsigned char* sw = smem + st * DSTAGE_BYTES + F::kXIn + js * 16 * (DN * 4) + nl * 4;
         uint32_t wd[3][16], s2[3];                // wd[q][row]: packed rows 0..15 of the group
 #pragma unroll
         for (int q = 0; q < 3; ++q) {
@@ -484,7 +553,8 @@ TcDecodePlan plan_dec(int M, int N, int K, int dev) {
   for (int S = 1; S <= 8 && S <= pl.ng; ++S) {
     const int range = (pl.ng + S - 1) / S;
     const int sbytes = kBits == 4 ? ((range + 7) / 8) * 8 * DSCALE_ROW : 0;
-    if (sbytes + 2 * DFmt<kBits>::kStage + 2048 > DSMEM_LIMIT) continue;   // scales + 2 stages must fit
+    // scales + 2 stages (+ 2 x slots) must fit
+    if (sbytes + 2 * (DFmt<kBits>::kStage + DX_STAGE - DFmt<kBits>::kXIn) + 2048 > DSMEM_LIMIT) continue;
     const int slots = dec_max_active_clusters<kBits>(S, dev);
     if (slots <= 0) continue;
     const long long waves = (pl.tiles + slots - 1) / slots;
@@ -524,9 +594,26 @@ cudaError_t launch_dec(const __half* x, const uint32_t* const w[3], const __half
   p.sbox = sbox;
   p.wait_ns = wait_ns;
   const int nstg = (range + DGPS - 1) / DGPS;
-  p.nst = std::min(std::min(nstg, DMAX_STAGES), (DSMEM_LIMIT - 1024 - sbytes) / F::kStage);
-  p.nst = std::max(p.nst, 1);
-  p.s_off = p.nst * F::kStage;
+  if constexpr (F::kSplitX) {
+    // as many stages as fit (up to DMAX_STAGES) with an x ring twice as deep
+    // (up to DMAX_X, never more than the CTA's stages)
+    p.nst = 1;
+    p.nx = std::min(nstg, 2);
+    for (int ns = std::min(nstg, DMAX_STAGES); ns >= 1; --ns) {
+      const int nx = std::max(1, std::min(nstg, std::min(DMAX_X, 2 * ns)));
+      if (ns * F::kStage + nx * DX_STAGE + sbytes + 1024 <= DSMEM_LIMIT) {
+        p.nst = ns;
+        p.nx = nx;
+        break;
+      }
+    }
+  } else {
+    p.nst = std::min(std::min(nstg, DMAX_STAGES), (DSMEM_LIMIT - 1024 - sbytes) / F::kStage);
+    p.nst = std::max(p.nst, 1);
+    p.nx = 1;                                     // x travels inside the stages
+  }
+  p.x_off = p.nst * F::kStage;
+  p.s_off = p.x_off + (F::kSplitX ? p.nx * DX_STAGE : 0);
   const size_t smem_used = static_cast<size_t>(p.s_off + sbytes + 1024);
   CUtensorMap tx, tw[3], ts[3];
   CUresult r = encode_tensor_map_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, x, K, M,
