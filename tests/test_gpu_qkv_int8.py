@@ -169,5 +169,13 @@ def test_input_written_by_the_preceding_kernel(m):
         assert_qkv_close(to_host(o), r, "x from preceding kernel")
 
 
+@pytest.mark.parametrize("m,n,k", [(1, 1032, 12416), (5, 264, 5760), (16, 136, 8576)])
+def test_decode_x_ring_wraps(m, n, k):
+    # M <= 16 keeps x in a ring of its own, four slots beside two weight
+    # stages: here each CTA's K range spans more stages than the x ring has
+    # slots, and K / 128 (97, 45, 67) is odd, so ranges end on half stages.
+    check_full(qkv_int8_inputs(m, n, k, seed=m + n + k), f"M={m} N={n} K={k}")
+
+
 def test_no_device_timeouts_reported():
     kaio.device_status()
