@@ -276,8 +276,13 @@ int kaio_dequantize_per_group(int q_dtype, int dtype, int32_t outer, int32_t axi
  *
  *   w  u32 [K/8, N],  s  f16 [K/128, N],  out  f16 [K, N]
  *   variant 0: the K-row-order routine of the tile kernel (M >= 17)
- *   variant 1: the paired-nibble routine of the decode kernel (M <= 16)
- * Errors: as kaio_qkv_project_int4 for K and N; variant not 0 or 1.
+ *   variant 1: the decode kernel's general, paired-nibble routine (M <= 16)
+ *   variant 2: the decode kernel's two-instruction routine (one LOP3 and one
+ *              f16x2 FMA per pair) wherever the word's scale s lies in
+ *              0 < s <= 65504 * 2^-20, the paired-nibble routine elsewhere
+ *              (the decode kernel takes it when all three scales of a warp's
+ *              32 columns are in range)
+ * Errors: as kaio_qkv_project_int4 for K and N; variant not 0, 1 or 2.
  */
 int kaio_dequant_int4_debug(const uint32_t* w, const void* s, void* out, uint32_t K, uint32_t N,
                             int variant, kaio_stream_t stream);

@@ -243,6 +243,13 @@ int check_projection(const Span* in, int n_in, const Span* out, uint64_t packed_
 
 }  // namespace
 
+namespace kaio {
+// tc_decode.cu: the decode kernel's two-instruction routine alone (debug
+// variant 2); declared here, its only caller.
+cudaError_t launch_dequant_fast_debug(const uint32_t* w, const __half* s, __half* out, int K, int N,
+                                      cudaStream_t stream);
+}  // namespace kaio
+
 extern "C" {
 
 const char* kaio_last_error(void) { return g_last_error.c_str(); }
@@ -622,8 +629,8 @@ int kaio_dequant_int4_debug(const uint32_t* w, const void* s, void* out, uint32_
   if (K % 128 != 0)
     return fail(KAIO_ERR_INVALID_VALUE, "K (%u) must be a multiple of group_size (128)", K);
   if (N % 8 != 0) return fail(KAIO_ERR_INVALID_VALUE, "N (%u) must be a multiple of 8", N);
-  if (variant != 0 && variant != 1)
-    return fail(KAIO_ERR_INVALID_VALUE, "variant (%d) must be 0 or 1", variant);
+  if (variant < 0 || variant > 2)
+    return fail(KAIO_ERR_INVALID_VALUE, "variant (%d) must be 0, 1 or 2", variant);
   KAIO_TRY(check_aligned(in, 2));
   KAIO_TRY(check_aligned(o, 1));
   KAIO_TRY(check_overlap(in, 2, o, 1));
@@ -633,9 +640,11 @@ int kaio_dequant_int4_debug(const uint32_t* w, const void* s, void* out, uint32_
   if (K == 0 || N == 0) return KAIO_OK;
   KAIO_TRY(check_on_device(in, 2, dev));
   KAIO_TRY(check_on_device(o, 1, dev));
-  cudaError_t e = kaio::launch_dequant_debug(w, static_cast<const __half*>(s),
-                                             static_cast<__half*>(out), static_cast<int>(K),
-                                             static_cast<int>(N), variant, stream);
+  cudaError_t e =
+      variant == 2 ? kaio::launch_dequant_fast_debug(w, static_cast<const __half*>(s), static_cast<__half*>(out),
+                                                     static_cast<int>(K), static_cast<int>(N), stream)
+                   : kaio::launch_dequant_debug(w, static_cast<const __half*>(s), static_cast<__half*>(out),
+                                                static_cast<int>(K), static_cast<int>(N), variant, stream);
   if (e != cudaSuccess) return cuda_fail(e, "dequant kernel launch");
   return KAIO_OK;
 }

@@ -49,6 +49,32 @@ constexpr int DXBOX = DM * 64 * 2;               // one 64-K x box, 16 rows, 128
 constexpr int DX_STAGE = DGPS * 2 * DXBOX;       // 8 KB
 constexpr int DMAX_STAGES = 4;
 constexpr int DMAX_X = 8;                        // INT8: x ring slots (one stage's x boxes each)
+
+// Two-instruction exact INT4 conversion, for scales 0 < s <= 65504 * 2^-20
+// (f16 bits 0x0001 .. 0x2BFF). With nibble pair j moved to bits 4..7 of each
+// f16 half, (w & 0x00F000F0) ^ 0x00800080 is the subnormal u * 2^-20 with
+// u = n + 8 (the sign bit flipped, as in the general routine), and
+// fma(u * 2^-20, s * 2^20, -8 s) rounds the exact value n * s once: it equals
+// RN_f16(n * s) bit for bit. s * 2^20 and -8 s are exact in f16 over that
+// range. s = 0 or s < 0 would give +0 where n * s is -0 for n <= 0 and is
+// left to the general routine, as are larger, infinite and NaN scales.
+constexpr uint32_t kFastMask = 0x00F000F0u, kFastMagic = 0x00800080u;
+__device__ __forceinline__ uint32_t hfma2_rn(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+__device__ __forceinline__ bool fast_scale(uint16_t sb) { return static_cast<uint32_t>(sb) - 1u < 0x2BFFu; }
+// s * 2^20 (two exact scalings by 1024.0) and -8 s, from s2 = {s, s}
+__device__ __forceinline__ void fast_consts(uint32_t s2, uint32_t& sh, uint32_t& sm8) {
+  sh = hmul2_rn(hmul2_rn(s2, 0x64006400u), 0x64006400u);
+  sm8 = hmul2_rn(s2, 0xC800C800u);
+}
+// Pair j (nibbles j and j + 4, the order of PairedNibbles) of packed word w.
+__device__ __forceinline__ uint32_t fast_pair(uint32_t w, int j, uint32_t sh, uint32_t sm8) {
+  const uint32_t src = j == 0 ? w << 4 : (j == 1 ? w : (j == 2 ? w >> 4 : w >> 8));   // pair j at bits 4..7
+  return hfma2_rn(and_xor<kFastMask>(src, kFastMagic), sh, sm8);
+}
 constexpr int DSCALE_ROW = 3 * DN * 2;           // the three scale rows of one K group: 768 B
 constexpr int DDQ_WARPS = 8;                     // 2 per TMEM lane quadrant
 constexpr int DMMA_WARPS = 3;                    // one per projection
@@ -399,14 +425,17 @@ __global__ void __launch_bounds__(DTHREADS, 1)
         const unsigned char* sc = scale_base + (gl >> 3) * p.sbox * DSCALE_ROW + (gl & 7) * (DN * 2);
         const unsigned char* sw = smem + st * DSTAGE_BYTES + F::kXIn + js * 16 * (DN * 4) + nl * 4;
         uint32_t wd[3][16], s2[3];                // wd[q][row]: packed rows 0..15 of the group
+        bool small = true;                        // all three scales in the two-instruction range
 #pragma unroll
         for (int q = 0; q < 3; ++q) {
           const uint16_t sb = *reinterpret_cast<const uint16_t*>(sc + q * p.sbox * DN * 2);
           s2[q] = half2_bits(sb, sb);
+          small = small && fast_scale(sb);
 #pragma unroll
           for (int r = 0; r < 16; ++r)
             wd[q][r] = *reinterpret_cast<const uint32_t*>(sw + q * DW_BOX + r * (DN * 4));
         }
+        const bool fast = __all_sync(0xffffffffu, small);   // the warp takes one routine
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[st]);   // this set's words of the stage are in registers
         if (!mbar_wait_lim(&a_empty[js], aph ^ 1, abort, &g_td_err, p.wait_ns)) { ok = false; break; }
@@ -419,16 +448,31 @@ __global__ void __launch_bounds__(DTHREADS, 1)
             // holds K pair jj of packed row hh*8 + 2*kk + rr (the A layout of an MMA
             // step); one 32-column store covers MMA steps 2*k2 and 2*k2+1
             uint32_t v[32];
+            if (fast) {
+              uint32_t sh, sm8;
+              fast_consts(s2[q], sh, sm8);
 #pragma unroll
-            for (int kx = 0; kx < 2; ++kx)
+              for (int kx = 0; kx < 2; ++kx)
 #pragma unroll
-              for (int hh = 0; hh < 2; ++hh)
+                for (int hh = 0; hh < 2; ++hh)
 #pragma unroll
-                for (int rr = 0; rr < 2; ++rr) {
-                  const PairedNibbles pn(wd[q][hh * 8 + 2 * (2 * k2 + kx) + rr]);
+                  for (int rr = 0; rr < 2; ++rr) {
+                    const uint32_t w = wd[q][hh * 8 + 2 * (2 * k2 + kx) + rr];
 #pragma unroll
-                  for (int jj = 0; jj < 4; ++jj) v[kx * 16 + hh * 8 + 4 * rr + jj] = pn.pair(jj, s2[q]);
-                }
+                    for (int jj = 0; jj < 4; ++jj) v[kx * 16 + hh * 8 + 4 * rr + jj] = fast_pair(w, jj, sh, sm8);
+                  }
+            } else {
+#pragma unroll
+              for (int kx = 0; kx < 2; ++kx)
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+                  for (int rr = 0; rr < 2; ++rr) {
+                    const PairedNibbles pn(wd[q][hh * 8 + 2 * (2 * k2 + kx) + rr]);
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj) v[kx * 16 + hh * 8 + 4 * rr + jj] = pn.pair(jj, s2[q]);
+                  }
+            }
             tmem_st32(tbase + q * 64 + k2 * 32, v);
           }
         tmem_st_wait();
@@ -658,6 +702,30 @@ cudaError_t launch_dec(const __half* x, const uint32_t* const w[3], const __half
   return cudaGetLastError();
 }
 
+
+// The dequant stage of the decode kernel alone, for bit-exact tests: each
+// packed word with the two-instruction routine where its scale allows, the
+// paired-nibble routine elsewhere; out[8r + i][n] in K-row order.
+__global__ void dequant_fast_debug_kernel(const uint32_t* __restrict__ w, const __half* __restrict__ s,
+                                          __half* __restrict__ out, int K, int N) {
+  const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const long long total = static_cast<long long>(K / 8) * N;
+  if (idx >= total) return;
+  const int r = static_cast<int>(idx / N), n = static_cast<int>(idx % N);
+  const uint32_t word = w[idx];
+  const uint16_t sb = __half_as_ushort(s[static_cast<size_t>(r / 16) * N + n]);
+  const uint32_t s2 = half2_bits(sb, sb);
+  uint32_t sh, sm8;
+  fast_consts(s2, sh, sm8);
+  const PairedNibbles pn(word);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t v = fast_scale(sb) ? fast_pair(word, j, sh, sm8) : pn.pair(j, s2);
+    out[static_cast<size_t>(8 * r + j) * N + n] = __ushort_as_half(static_cast<uint16_t>(v & 0xFFFFu));
+    out[static_cast<size_t>(8 * r + j + 4) * N + n] = __ushort_as_half(static_cast<uint16_t>(v >> 16));
+  }
+}
+
 }  // namespace
 
 // The plan depends on (device, N, K, M <= 16) only; the last few are kept per
@@ -710,6 +778,16 @@ unsigned read_and_clear_tc_decode_errors() {
   const unsigned zero = 0;
   cudaMemcpyToSymbol(g_td_err, &zero, sizeof(zero));
   return v;
+}
+
+cudaError_t launch_dequant_fast_debug(const uint32_t* w, const __half* s, __half* out, int K, int N,
+                                      cudaStream_t stream) {
+  const long long total = static_cast<long long>(K / 8) * N;
+  if (total == 0) return cudaSuccess;
+  const int threads = 256;
+  const long long blocks = (total + threads - 1) / threads;
+  dequant_fast_debug_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(w, s, out, K, N);
+  return cudaGetLastError();
 }
 
 }  // namespace kaio

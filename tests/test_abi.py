@@ -120,7 +120,8 @@ def test_matmul_validation(L):
 
 
 def test_dequant_debug_validation(L):
-    assert L.kaio_dequant_int4_debug(ptr(0), ptr(1), ptr(2), 128, 64, 2, None) == INVALID
+    assert L.kaio_dequant_int4_debug(ptr(0), ptr(1), ptr(2), 128, 64, 3, None) == INVALID
+    assert L.kaio_dequant_int4_debug(ptr(0), ptr(1), ptr(2), 128, 64, -1, None) == INVALID
     assert L.kaio_dequant_int4_debug(ptr(0), ptr(1), ptr(2), 100, 64, 0, None) == INVALID
     assert L.kaio_dequant_int4_debug(ptr(0), ptr(1), ptr(0), 128, 64, 0, None) == INVALID
 
