@@ -222,3 +222,17 @@ def test_decode_rows_not_a_multiple_of_the_cluster(m):
     # multiple of S some ranks finish fewer rows than others (here K = 8192 over
     # 64 groups and a ragged last column tile).
     check_full(qkv_inputs(m, 1032, 8192, seed=100 + m), f"M={m} N=1032 K=8192")
+
+
+@pytest.mark.parametrize("m", [1, 16])
+def test_decode_more_ctas_than_sms(m):
+    # N = 20480 is 160 column tiles: with K = 384 the planner runs them as 160
+    # single-CTA clusters, more than the GPU's 152 SMs hold at once, so CTAs of
+    # a second wave start as the first ones finish (and programmatic launch
+    # lets the next call's CTAs wait on this one's).
+    inp = qkv_inputs(m, 20480, 384, seed=20480 + m)
+    got = run(inp)
+    got2 = run(inp)
+    for g, g2, r, name in zip(got, got2, oracle.qkv_project_int4_ref(*inp.__dict__.values()), "QKV"):
+        assert_qkv_close(g, r, f"M={m} N=20480 {name}")
+        assert np.array_equal(g.view(np.uint16), g2.view(np.uint16))

@@ -177,5 +177,11 @@ def test_decode_x_ring_wraps(m, n, k):
     check_full(qkv_int8_inputs(m, n, k, seed=m + n + k), f"M={m} N={n} K={k}")
 
 
+@pytest.mark.parametrize("m", [1, 16])
+def test_decode_more_ctas_than_sms(m):
+    # 160 column tiles of single-CTA clusters: two waves on a 152-SM GPU
+    check_full(qkv_int8_inputs(m, 20480, 384, seed=20480 + m), f"M={m} N=20480 K=384")
+
+
 def test_no_device_timeouts_reported():
     kaio.device_status()
