@@ -451,6 +451,10 @@ __global__ void __launch_bounds__(DTHREADS, 1)
             if (fast) {
               uint32_t sh, sm8;
               fast_consts(s2[q], sh, sm8);
+              // in two passes (the 32 LOP3, then the 32 FMAs), so that each warp
+              // has independent instructions to issue while results are in
+              // flight: two dequant warps per scheduler hide little latency
+              // (M=16, K=N=8192: 29.35 -> 29.11 us)
 #pragma unroll
               for (int kx = 0; kx < 2; ++kx)
 #pragma unroll
@@ -458,9 +462,15 @@ __global__ void __launch_bounds__(DTHREADS, 1)
 #pragma unroll
                   for (int rr = 0; rr < 2; ++rr) {
                     const uint32_t w = wd[q][hh * 8 + 2 * (2 * k2 + kx) + rr];
+                    const uint32_t src[4] = {w << 4, w, w >> 4, w >> 8};   // pair j at bits 4..7
 #pragma unroll
-                    for (int jj = 0; jj < 4; ++jj) v[kx * 16 + hh * 8 + 4 * rr + jj] = fast_pair(w, jj, sh, sm8);
+                    for (int jj = 0; jj < 4; ++jj)
+                      v[kx * 16 + hh * 8 + 4 * rr + jj] = and_xor<kFastMask>(src[jj], kFastMagic);
                   }
+#pragma unroll
+              for (int c = 0; c < 32; ++c) asm volatile("" : "+r"(v[c]));   // keep the passes apart
+#pragma unroll
+              for (int c = 0; c < 32; ++c) v[c] = hfma2_rn(v[c], sh, sm8);
             } else {
 #pragma unroll
               for (int kx = 0; kx < 2; ++kx)
